@@ -1,0 +1,207 @@
+"""CPU oracle for the FP8 (E4M3) groupwise-scaled NT GEMM — TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+may import this package.  The CUDA library never does: it shares no code with
+the oracle, and the product path fails instead of falling back to it.
+
+The arithmetic lives in ``oracle.c`` (plain C, FP64, one rounding); this module
+only marshals numpy arrays (or CPU torch tensors) into it.  It follows the MATE
+page "FlashInfer Wrapper APIs", section GEMM: ``gemm_fp8_nt_groupwise``,
+``group_deepgemm_fp8_nt_groupwise`` and ``batch_deepgemm_fp8_nt_groupwise``.
+"""
+import ctypes
+
+import numpy as np
+
+from . import build as _build
+
+OUT_BF16 = 0
+OUT_F16 = 1
+SCALE_K_MAJOR = 0
+SCALE_MN_MAJOR = 1
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(_build.build())
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        I = ctypes.c_int
+        lib.oracle_e4m3_table.argtypes = [P]
+        lib.oracle_e4m3_table.restype = None
+        lib.oracle_round.argtypes = [P, I64, I, P, P]
+        lib.oracle_round.restype = None
+        lib.oracle_gemm_nt_groupwise.argtypes = [P, P, P, P, I64, I64, I64, I, I, P, P]
+        lib.oracle_gemm_nt_groupwise_at.argtypes = [P, P, P, P, I64, I64, I64, I, I,
+                                                    P, P, I64, P, P]
+        lib.oracle_group_gemm_contiguous.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
+                                                     P, P, P]
+        lib.oracle_group_gemm_contiguous_at.argtypes = [P, P, P, P, P, I64, I64, I64,
+                                                        I64, P, P, I64, P, P, P]
+        lib.oracle_batch_gemm_masked.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
+                                                 P, P, P]
+        lib.oracle_batch_gemm_masked_at.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
+                                                    P, P, P, I64, P, P, P]
+        for f in ("oracle_gemm_nt_groupwise", "oracle_gemm_nt_groupwise_at",
+                  "oracle_group_gemm_contiguous", "oracle_group_gemm_contiguous_at",
+                  "oracle_batch_gemm_masked", "oracle_batch_gemm_masked_at",
+                  "oracle_num_threads"):
+            getattr(lib, f).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _arr(x, dtype):
+    """A C-contiguous numpy array of `dtype` viewing or copying `x`."""
+    if hasattr(x, "detach"):  # torch tensor
+        t = x.detach().cpu().contiguous()
+        if t.element_size() == 1 and dtype == np.uint8:
+            import torch
+            t = t.view(torch.uint8)
+        x = t.numpy()
+    a = np.ascontiguousarray(x)
+    if a.dtype != dtype:
+        if dtype == np.uint8:
+            raise TypeError("E4M3 operands must be 1-byte codes, got %s" % a.dtype)
+        a = a.astype(dtype)
+    return a
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def _check(rc, what):
+    if rc == -2:
+        raise ValueError("%s: m_indices violates the page's contiguous-layout "
+                         "precondition" % what)
+    if rc != 0:
+        raise ValueError("%s: invalid arguments" % what)
+
+
+def num_threads():
+    return _load().oracle_num_threads()
+
+
+def e4m3_table():
+    """The 256 E4M3 code values (FP64), NaN at 0x7F and 0xFF."""
+    out = np.empty(256, np.float64)
+    _load().oracle_e4m3_table(out.ctypes.data)
+    return out
+
+
+def round_to(x, out_dtype=OUT_BF16):
+    """Round FP64 values once (nearest, ties to even) to BF16/FP16.
+
+    Returns ``(rounded_values_f64, bits_u16)``.
+    """
+    x = _arr(x, np.float64)
+    y = np.empty_like(x)
+    bits = np.empty(x.shape, np.uint16)
+    _load().oracle_round(x.ctypes.data, x.size, out_dtype, y.ctypes.data,
+                         bits.ctypes.data)
+    return y, bits
+
+
+def gemm_nt_groupwise(a, b, a_scale, b_scale, scale_major=SCALE_K_MAJOR,
+                      out_dtype=OUT_BF16):
+    """Dense form: returns ``(ref_f64 (m,n), bits_u16 (m,n))``."""
+    a, b = _arr(a, np.uint8), _arr(b, np.uint8)
+    sa, sb = _arr(a_scale, np.float32), _arr(b_scale, np.float32)
+    m, k = a.shape
+    n = b.shape[0]
+    ref = np.empty((m, n), np.float64)
+    bits = np.empty((m, n), np.uint16)
+    rc = _load().oracle_gemm_nt_groupwise(_p(a), _p(b), _p(sa), _p(sb), m, n, k,
+                                          scale_major, out_dtype, _p(ref), _p(bits))
+    _check(rc, "gemm_nt_groupwise")
+    return ref, bits
+
+
+def gemm_nt_groupwise_at(a, b, a_scale, b_scale, rows, cols,
+                         scale_major=SCALE_K_MAJOR, out_dtype=OUT_BF16):
+    """Dense form at positions (rows[s], cols[s]): ``(ref_f64, bits_u16)``."""
+    a, b = _arr(a, np.uint8), _arr(b, np.uint8)
+    sa, sb = _arr(a_scale, np.float32), _arr(b_scale, np.float32)
+    rows, cols = _arr(rows, np.int64).ravel(), _arr(cols, np.int64).ravel()
+    m, k = a.shape
+    n = b.shape[0]
+    ref = np.empty(rows.size, np.float64)
+    bits = np.empty(rows.size, np.uint16)
+    rc = _load().oracle_gemm_nt_groupwise_at(
+        _p(a), _p(b), _p(sa), _p(sb), m, n, k, scale_major, out_dtype,
+        _p(rows), _p(cols), rows.size, _p(ref), _p(bits))
+    _check(rc, "gemm_nt_groupwise_at")
+    return ref, bits
+
+
+def group_gemm_contiguous(a, b, a_scale, b_scale, m_indices):
+    """Contiguous grouped form: ``(ref_f64, bits_u16, written_bool)``, (m,n)."""
+    a, b = _arr(a, np.uint8), _arr(b, np.uint8)
+    sa, sb = _arr(a_scale, np.float32), _arr(b_scale, np.float32)
+    mi = _arr(m_indices, np.int32)
+    m, k = a.shape
+    g, n = b.shape[0], b.shape[1]
+    ref = np.zeros((m, n), np.float64)
+    bits = np.zeros((m, n), np.uint16)
+    written = np.zeros((m, n), np.uint8)
+    rc = _load().oracle_group_gemm_contiguous(
+        _p(a), _p(b), _p(sa), _p(sb), _p(mi), m, n, k, g, _p(ref), _p(bits),
+        _p(written))
+    _check(rc, "group_gemm_contiguous")
+    return ref, bits, written.astype(bool)
+
+
+def group_gemm_contiguous_at(a, b, a_scale, b_scale, m_indices, rows, cols):
+    a, b = _arr(a, np.uint8), _arr(b, np.uint8)
+    sa, sb = _arr(a_scale, np.float32), _arr(b_scale, np.float32)
+    mi = _arr(m_indices, np.int32)
+    rows, cols = _arr(rows, np.int64).ravel(), _arr(cols, np.int64).ravel()
+    m, k = a.shape
+    g, n = b.shape[0], b.shape[1]
+    ref = np.zeros(rows.size, np.float64)
+    bits = np.zeros(rows.size, np.uint16)
+    written = np.zeros(rows.size, np.uint8)
+    rc = _load().oracle_group_gemm_contiguous_at(
+        _p(a), _p(b), _p(sa), _p(sb), _p(mi), m, n, k, g, _p(rows), _p(cols),
+        rows.size, _p(ref), _p(bits), _p(written))
+    _check(rc, "group_gemm_contiguous_at")
+    return ref, bits, written.astype(bool)
+
+
+def batch_gemm_masked(a, b, a_scale, b_scale, masked_m):
+    """Masked batched form: ``(ref_f64, bits_u16, written_bool)``, (G,max_m,n)."""
+    a, b = _arr(a, np.uint8), _arr(b, np.uint8)
+    sa, sb = _arr(a_scale, np.float32), _arr(b_scale, np.float32)
+    mm = _arr(masked_m, np.int32)
+    g, max_m, k = a.shape
+    n = b.shape[1]
+    ref = np.zeros((g, max_m, n), np.float64)
+    bits = np.zeros((g, max_m, n), np.uint16)
+    written = np.zeros((g, max_m, n), np.uint8)
+    rc = _load().oracle_batch_gemm_masked(
+        _p(a), _p(b), _p(sa), _p(sb), _p(mm), g, max_m, n, k, _p(ref), _p(bits),
+        _p(written))
+    _check(rc, "batch_gemm_masked")
+    return ref, bits, written.astype(bool)
+
+
+def batch_gemm_masked_at(a, b, a_scale, b_scale, masked_m, groups, rows, cols):
+    a, b = _arr(a, np.uint8), _arr(b, np.uint8)
+    sa, sb = _arr(a_scale, np.float32), _arr(b_scale, np.float32)
+    mm = _arr(masked_m, np.int32)
+    groups = _arr(groups, np.int64).ravel()
+    rows, cols = _arr(rows, np.int64).ravel(), _arr(cols, np.int64).ravel()
+    g, max_m, k = a.shape
+    n = b.shape[1]
+    ref = np.zeros(rows.size, np.float64)
+    bits = np.zeros(rows.size, np.uint16)
+    written = np.zeros(rows.size, np.uint8)
+    rc = _load().oracle_batch_gemm_masked_at(
+        _p(a), _p(b), _p(sa), _p(sb), _p(mm), g, max_m, n, k, _p(groups),
+        _p(rows), _p(cols), rows.size, _p(ref), _p(bits), _p(written))
+    _check(rc, "batch_gemm_masked_at")
+    return ref, bits, written.astype(bool)

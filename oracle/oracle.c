@@ -1,0 +1,452 @@
+/*
+ * CPU oracle for the FP8 (E4M3) groupwise-scaled NT GEMM — TEST INFRASTRUCTURE.
+ *
+ * Plain, slow and written to be checked by eye against the definition on the
+ * MATE page "FlashInfer Wrapper APIs", section GEMM (gemm_fp8_nt_groupwise,
+ * group_deepgemm_fp8_nt_groupwise, batch_deepgemm_fp8_nt_groupwise).  No
+ * blocking, no reordering: one output element at a time, one 128-wide K block
+ * at a time, in FP64, then one rounding.  The only parallelism is over output
+ * elements, which does not change any arithmetic.
+ *
+ * Built with -ffp-contract=off so that no multiply-add is fused and the
+ * results are the same on every host.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stddef.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define KBLOCK 128 /* scale granularity along k, (1, 128, 128) */
+#define NBLOCK 128 /* scale granularity along n */
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* E4M3 as named by the page (torch.float8_e4m3fn): sign s, exponent field e
+ * (bias 7), mantissa field f.  e == 0 is subnormal: f * 2^-3 * 2^(1-7).
+ * Otherwise (1 + f/8) * 2^(e-7).  e == 15 with f == 7 is NaN; there is no
+ * infinity, so e == 15 with f < 7 are ordinary finite values (max 448). */
+void oracle_e4m3_table(double out[256])
+{
+    for (int c = 0; c < 256; ++c) {
+        int s = (c >> 7) & 1;
+        int e = (c >> 3) & 15;
+        int f = c & 7;
+        double v;
+        if (e == 15 && f == 7)
+            v = NAN;
+        else if (e == 0)
+            v = ldexp((double)f, -9);
+        else
+            v = ldexp((double)(8 + f), e - 10);
+        out[c] = s ? -v : v;
+    }
+}
+
+/* Round to nearest, ties to even, into a binary format with p significand
+ * bits (including the implicit one), smallest normal exponent emin and
+ * largest finite value maxfinite.  The rounding quantum is 2^(E - p + 1) with
+ * E the exponent of the leading bit of |x| (floored at emin for subnormals);
+ * dividing by it is exact, nearbyint() rounds to even in the default mode. */
+static double round_to_format(double x, int p, int emin, double maxfinite)
+{
+    if (isnan(x) || isinf(x) || x == 0.0)
+        return x;
+    int e2;
+    frexp(fabs(x), &e2); /* |x| = f * 2^e2, f in [0.5, 1) */
+    int lead = e2 - 1;
+    if (lead < emin)
+        lead = emin;
+    double quantum = ldexp(1.0, lead - (p - 1));
+    double y = nearbyint(x / quantum) * quantum;
+    if (fabs(y) > maxfinite)
+        return copysign(INFINITY, x);
+    return y;
+}
+
+#define BF16_P 8
+#define BF16_EMIN (-126)
+#define BF16_MAX 3.3895313892515355e38 /* (2 - 2^-7) * 2^127 */
+#define F16_P 11
+#define F16_EMIN (-14)
+#define F16_MAX 65504.0
+
+/* 16-bit encodings of a value that is already representable in the format. */
+static uint16_t encode_bf16(double y)
+{
+    if (isnan(y))
+        return (uint16_t)0x7FC0;
+    union {
+        float f;
+        uint32_t u;
+    } v;
+    v.f = (float)y; /* exact: every BF16 value is an FP32 value */
+    return (uint16_t)(v.u >> 16);
+}
+
+static uint16_t encode_f16(double y)
+{
+    if (isnan(y))
+        return (uint16_t)0x7E00;
+    uint16_t sign = signbit(y) ? 0x8000 : 0;
+    double a = fabs(y);
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7C00);
+    if (a == 0.0)
+        return sign;
+    if (a < ldexp(1.0, F16_EMIN)) /* subnormal: a = mant * 2^-24 */
+        return (uint16_t)(sign | (uint16_t)ldexp(a, 24));
+    int e2;
+    frexp(a, &e2);
+    int lead = e2 - 1; /* a = (1 + mant/1024) * 2^lead */
+    uint16_t mant = (uint16_t)(ldexp(a, 10 - lead) - 1024.0);
+    return (uint16_t)(sign | (uint16_t)((lead + 15) << 10) | mant);
+}
+
+static double round_one(double x, int out_dtype, uint16_t* bits)
+{
+    double y;
+    if (out_dtype == ORACLE_OUT_F16) {
+        y = round_to_format(x, F16_P, F16_EMIN, F16_MAX);
+        if (bits)
+            *bits = encode_f16(y);
+    } else {
+        y = round_to_format(x, BF16_P, BF16_EMIN, BF16_MAX);
+        if (bits)
+            *bits = encode_bf16(y);
+    }
+    return y;
+}
+
+void oracle_round(const double* x, int64_t count, int out_dtype,
+                  double* rounded, uint16_t* bits)
+{
+    for (int64_t s = 0; s < count; ++s) {
+        double y = round_one(x[s], out_dtype, bits ? bits + s : NULL);
+        if (rounded)
+            rounded[s] = y;
+    }
+}
+
+/* One output element of the definition.  arow/brow are the k codes of row i
+ * of a and row j of b; sa[kb*sa_step] and sb[kb*sb_step] are the scales of
+ * K block kb for that row of a and that 128-column block of b. */
+static double element(const double* dec, const uint8_t* arow,
+                      const uint8_t* brow, const float* sa, int64_t sa_step,
+                      const float* sb, int64_t sb_step, int64_t kblocks)
+{
+    double r = 0.0;
+    for (int64_t kb = 0; kb < kblocks; ++kb) {
+        double p = 0.0; /* exact block sum */
+        for (int64_t t = kb * KBLOCK; t < (kb + 1) * KBLOCK; ++t)
+            p += dec[arow[t]] * dec[brow[t]];
+        double scale = (double)sa[kb * sa_step] * (double)sb[kb * sb_step];
+        r += p * scale;
+    }
+    return r;
+}
+
+static int check_dense_shape(int64_t m, int64_t n, int64_t k, int scale_major,
+                             int out_dtype)
+{
+    if (m < 0 || n <= 0 || k <= 0 || n % NBLOCK || k % KBLOCK)
+        return -1;
+    if (scale_major != ORACLE_SCALE_K_MAJOR &&
+        scale_major != ORACLE_SCALE_MN_MAJOR)
+        return -1;
+    if (out_dtype != ORACLE_OUT_BF16 && out_dtype != ORACLE_OUT_F16)
+        return -1;
+    return 0;
+}
+
+/* Dense element (i, j) with the scale layout of the page: K-major
+ * a_scale[i][kb], b_scale[j/128][kb]; MN-major a_scale[kb][i],
+ * b_scale[kb][j/128]. */
+static double dense_element(const double* dec, const uint8_t* a,
+                            const uint8_t* b, const float* a_scale,
+                            const float* b_scale, int64_t m, int64_t n,
+                            int64_t k, int scale_major, int64_t i, int64_t j)
+{
+    int64_t kblocks = k / KBLOCK, nblocks = n / NBLOCK, jb = j / NBLOCK;
+    const float *sa, *sb;
+    int64_t sa_step, sb_step;
+    if (scale_major == ORACLE_SCALE_K_MAJOR) {
+        sa = a_scale + i * kblocks;
+        sa_step = 1;
+        sb = b_scale + jb * kblocks;
+        sb_step = 1;
+    } else {
+        sa = a_scale + i;
+        sa_step = m;
+        sb = b_scale + jb;
+        sb_step = nblocks;
+    }
+    return element(dec, a + i * k, b + j * k, sa, sa_step, sb, sb_step,
+                   kblocks);
+}
+
+int oracle_gemm_nt_groupwise(const uint8_t* a, const uint8_t* b,
+                             const float* a_scale, const float* b_scale,
+                             int64_t m, int64_t n, int64_t k, int scale_major,
+                             int out_dtype, double* ref, uint16_t* out)
+{
+    if (check_dense_shape(m, n, k, scale_major, out_dtype))
+        return -1;
+    double dec[256];
+    oracle_e4m3_table(dec);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < m; ++i) {
+        for (int64_t j = 0; j < n; ++j) {
+            double r = dense_element(dec, a, b, a_scale, b_scale, m, n, k,
+                                     scale_major, i, j);
+            uint16_t bits;
+            round_one(r, out_dtype, &bits);
+            if (ref)
+                ref[i * n + j] = r;
+            if (out)
+                out[i * n + j] = bits;
+        }
+    }
+    return 0;
+}
+
+int oracle_gemm_nt_groupwise_at(const uint8_t* a, const uint8_t* b,
+                                const float* a_scale, const float* b_scale,
+                                int64_t m, int64_t n, int64_t k, int scale_major,
+                                int out_dtype, const int64_t* rows,
+                                const int64_t* cols, int64_t count,
+                                double* ref, uint16_t* out)
+{
+    if (check_dense_shape(m, n, k, scale_major, out_dtype) || count < 0)
+        return -1;
+    for (int64_t s = 0; s < count; ++s)
+        if (rows[s] < 0 || rows[s] >= m || cols[s] < 0 || cols[s] >= n)
+            return -1;
+    double dec[256];
+    oracle_e4m3_table(dec);
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t s = 0; s < count; ++s) {
+        double r = dense_element(dec, a, b, a_scale, b_scale, m, n, k,
+                                 scale_major, rows[s], cols[s]);
+        uint16_t bits;
+        round_one(r, out_dtype, &bits);
+        if (ref)
+            ref[s] = r;
+        if (out)
+            out[s] = bits;
+    }
+    return 0;
+}
+
+/* The page requires each expert's rows to sit in a contiguous region aligned
+ * to 128 rows, with -1 marking padding.  So every 128-row block holds rows of
+ * at most one expert; ids outside [-1, G) or two experts in one block are a
+ * precondition violation. */
+static int check_m_indices(const int32_t* m_indices, int64_t m,
+                           int64_t num_groups)
+{
+    for (int64_t i0 = 0; i0 < m; i0 += 128) {
+        int32_t expert = -1;
+        for (int64_t i = i0; i < m && i < i0 + 128; ++i) {
+            int32_t e = m_indices[i];
+            if (e < -1 || e >= num_groups)
+                return -1;
+            if (e == -1)
+                continue;
+            if (expert != -1 && e != expert)
+                return -1;
+            expert = e;
+        }
+    }
+    return 0;
+}
+
+/* Grouped element: row i of a against row j of expert e's weights. */
+static double grouped_element(const double* dec, const uint8_t* a,
+                              const uint8_t* b, const float* a_scale,
+                              const float* b_scale, int64_t n, int64_t k,
+                              int32_t e, int64_t i, int64_t j)
+{
+    int64_t kblocks = k / KBLOCK, nblocks = n / NBLOCK;
+    const uint8_t* be = b + (int64_t)e * n * k;
+    const float* sbe = b_scale + (int64_t)e * nblocks * kblocks;
+    return element(dec, a + i * k, be + j * k, a_scale + i * kblocks, 1,
+                   sbe + (j / NBLOCK) * kblocks, 1, kblocks);
+}
+
+int oracle_group_gemm_contiguous(const uint8_t* a, const uint8_t* b,
+                                 const float* a_scale, const float* b_scale,
+                                 const int32_t* m_indices, int64_t m, int64_t n,
+                                 int64_t k, int64_t num_groups, double* ref,
+                                 uint16_t* out, uint8_t* written)
+{
+    if (check_dense_shape(m, n, k, ORACLE_SCALE_K_MAJOR, ORACLE_OUT_BF16) ||
+        num_groups <= 0)
+        return -1;
+    if (check_m_indices(m_indices, m, num_groups))
+        return -2;
+    double dec[256];
+    oracle_e4m3_table(dec);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < m; ++i) {
+        int32_t e = m_indices[i];
+        if (written)
+            for (int64_t j = 0; j < n; ++j)
+                written[i * n + j] = (uint8_t)(e != -1);
+        if (e == -1)
+            continue;
+        for (int64_t j = 0; j < n; ++j) {
+            double r = grouped_element(dec, a, b, a_scale, b_scale, n, k, e,
+                                       i, j);
+            uint16_t bits;
+            round_one(r, ORACLE_OUT_BF16, &bits);
+            if (ref)
+                ref[i * n + j] = r;
+            if (out)
+                out[i * n + j] = bits;
+        }
+    }
+    return 0;
+}
+
+int oracle_group_gemm_contiguous_at(const uint8_t* a, const uint8_t* b,
+                                    const float* a_scale, const float* b_scale,
+                                    const int32_t* m_indices, int64_t m,
+                                    int64_t n, int64_t k, int64_t num_groups,
+                                    const int64_t* rows, const int64_t* cols,
+                                    int64_t count, double* ref, uint16_t* out,
+                                    uint8_t* written)
+{
+    if (check_dense_shape(m, n, k, ORACLE_SCALE_K_MAJOR, ORACLE_OUT_BF16) ||
+        num_groups <= 0 || count < 0)
+        return -1;
+    if (check_m_indices(m_indices, m, num_groups))
+        return -2;
+    for (int64_t s = 0; s < count; ++s)
+        if (rows[s] < 0 || rows[s] >= m || cols[s] < 0 || cols[s] >= n)
+            return -1;
+    double dec[256];
+    oracle_e4m3_table(dec);
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t s = 0; s < count; ++s) {
+        int32_t e = m_indices[rows[s]];
+        if (written)
+            written[s] = (uint8_t)(e != -1);
+        if (e == -1)
+            continue;
+        double r = grouped_element(dec, a, b, a_scale, b_scale, n, k, e,
+                                   rows[s], cols[s]);
+        uint16_t bits;
+        round_one(r, ORACLE_OUT_BF16, &bits);
+        if (ref)
+            ref[s] = r;
+        if (out)
+            out[s] = bits;
+    }
+    return 0;
+}
+
+/* Valid rows of group g: masked_m[g] clamped to [0, max_m]. */
+static int64_t valid_rows(const int32_t* masked_m, int64_t g, int64_t max_m)
+{
+    int64_t v = masked_m[g];
+    if (v < 0)
+        v = 0;
+    if (v > max_m)
+        v = max_m;
+    return v;
+}
+
+static double masked_element(const double* dec, const uint8_t* a,
+                             const uint8_t* b, const float* a_scale,
+                             const float* b_scale, int64_t max_m, int64_t n,
+                             int64_t k, int64_t g, int64_t r, int64_t j)
+{
+    int64_t kblocks = k / KBLOCK, nblocks = n / NBLOCK;
+    int64_t row = g * max_m + r;
+    return element(dec, a + row * k, b + (g * n + j) * k,
+                   a_scale + row * kblocks, 1,
+                   b_scale + (g * nblocks + j / NBLOCK) * kblocks, 1, kblocks);
+}
+
+int oracle_batch_gemm_masked(const uint8_t* a, const uint8_t* b,
+                             const float* a_scale, const float* b_scale,
+                             const int32_t* masked_m, int64_t num_groups,
+                             int64_t max_m, int64_t n, int64_t k, double* ref,
+                             uint16_t* out, uint8_t* written)
+{
+    if (check_dense_shape(max_m, n, k, ORACLE_SCALE_K_MAJOR, ORACLE_OUT_BF16) ||
+        num_groups < 0)
+        return -1;
+    double dec[256];
+    oracle_e4m3_table(dec);
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t g = 0; g < num_groups; ++g) {
+        for (int64_t r = 0; r < max_m; ++r) {
+            int64_t base = (g * max_m + r) * n;
+            int valid = r < valid_rows(masked_m, g, max_m);
+            if (written)
+                for (int64_t j = 0; j < n; ++j)
+                    written[base + j] = (uint8_t)valid;
+            if (!valid)
+                continue;
+            for (int64_t j = 0; j < n; ++j) {
+                double x = masked_element(dec, a, b, a_scale, b_scale, max_m,
+                                          n, k, g, r, j);
+                uint16_t bits;
+                round_one(x, ORACLE_OUT_BF16, &bits);
+                if (ref)
+                    ref[base + j] = x;
+                if (out)
+                    out[base + j] = bits;
+            }
+        }
+    }
+    return 0;
+}
+
+int oracle_batch_gemm_masked_at(const uint8_t* a, const uint8_t* b,
+                                const float* a_scale, const float* b_scale,
+                                const int32_t* masked_m, int64_t num_groups,
+                                int64_t max_m, int64_t n, int64_t k,
+                                const int64_t* groups, const int64_t* rows,
+                                const int64_t* cols, int64_t count, double* ref,
+                                uint16_t* out, uint8_t* written)
+{
+    if (check_dense_shape(max_m, n, k, ORACLE_SCALE_K_MAJOR, ORACLE_OUT_BF16) ||
+        num_groups < 0 || count < 0)
+        return -1;
+    for (int64_t s = 0; s < count; ++s)
+        if (groups[s] < 0 || groups[s] >= num_groups || rows[s] < 0 ||
+            rows[s] >= max_m || cols[s] < 0 || cols[s] >= n)
+            return -1;
+    double dec[256];
+    oracle_e4m3_table(dec);
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t s = 0; s < count; ++s) {
+        int valid = rows[s] < valid_rows(masked_m, groups[s], max_m);
+        if (written)
+            written[s] = (uint8_t)valid;
+        if (!valid)
+            continue;
+        double x = masked_element(dec, a, b, a_scale, b_scale, max_m, n, k,
+                                  groups[s], rows[s], cols[s]);
+        uint16_t bits;
+        round_one(x, ORACLE_OUT_BF16, &bits);
+        if (ref)
+            ref[s] = x;
+        if (out)
+            out[s] = bits;
+    }
+    return 0;
+}

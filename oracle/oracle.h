@@ -1,0 +1,123 @@
+/*
+ * CPU oracle for the FP8 (E4M3) groupwise-scaled NT GEMM and its two MoE forms.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link or
+ * call this code: only the test suite, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header, table or helper with the
+ * CUDA library.
+ *
+ * What it computes is the plain definition of the operation on the MATE page
+ * "FlashInfer Wrapper APIs", section GEMM:
+ *   - gemm_fp8_nt_groupwise:            out = a @ b.T with FP32 scales at
+ *                                       granularity (1, 128, 128)
+ *   - group_deepgemm_fp8_nt_groupwise:  out[i] = a[i] @ b[m_indices[i]].T
+ *   - batch_deepgemm_fp8_nt_groupwise:  out[g, :masked_m[g]] =
+ *                                       a[g, :masked_m[g]] @ b[g].T
+ *
+ * With dec() the E4M3 decode, KB = k/128 and sa/sb the scales:
+ *   P(i,j,kb) = sum_{t in block kb} dec(a[i,t]) * dec(b[j,t])          (FP64)
+ *   R(i,j)    = sum_kb P(i,j,kb) * ((double)sa(i,kb) * (double)sb(j/128,kb))
+ *   out(i,j)  = R(i,j) rounded once, to nearest even, to BF16 or FP16.
+ *
+ * Each block sum P is exact in FP64 (every E4M3 value is an integer multiple
+ * of 2^-9 no larger than 448, so a 128-term sum of products needs < 44
+ * significant bits), and so is the scale product (24 + 24 bits).  The only
+ * roundings are the FP64 sum over K blocks and the final conversion.
+ *
+ * Every function returns 0 on success and a negative value if its arguments
+ * violate a precondition of the page (bad shape, m_indices outside [-1, G),
+ * an expert id that changes inside a 128-row block).
+ */
+#ifndef FP8G_ORACLE_H
+#define FP8G_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Output formats of the final rounding. */
+#define ORACLE_OUT_BF16 0
+#define ORACLE_OUT_F16 1
+
+/* Scale layouts: K-major a_scale (m, k/128), b_scale (n/128, k/128);
+ * MN-major a_scale (k/128, m), b_scale (k/128, n/128). */
+#define ORACLE_SCALE_K_MAJOR 0
+#define ORACLE_SCALE_MN_MAJOR 1
+
+/* The 256-entry E4M3 (float8_e4m3fn) decode table, built from the format
+ * definition: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, exponent 1111 with mantissa 111 is NaN. */
+void oracle_e4m3_table(double out[256]);
+
+/* Round x once, to nearest with ties to even, to BF16 or FP16.  Writes the
+ * rounded value (as a double) and its 16-bit encoding.  Overflow gives +-inf
+ * under the usual round-to-nearest rule, NaN stays NaN. */
+void oracle_round(const double* x, int64_t count, int out_dtype,
+                  double* rounded, uint16_t* bits);
+
+/* Dense form.  a (m,k) and b (n,k) are row-major E4M3 codes.  ref (m*n) gets
+ * R before rounding, out (m*n) the rounded 16-bit codes; either may be NULL. */
+int oracle_gemm_nt_groupwise(const uint8_t* a, const uint8_t* b,
+                             const float* a_scale, const float* b_scale,
+                             int64_t m, int64_t n, int64_t k, int scale_major,
+                             int out_dtype, double* ref, uint16_t* out);
+
+/* Dense form at `count` chosen positions (rows[s], cols[s]); ref/out have
+ * `count` entries. */
+int oracle_gemm_nt_groupwise_at(const uint8_t* a, const uint8_t* b,
+                                const float* a_scale, const float* b_scale,
+                                int64_t m, int64_t n, int64_t k, int scale_major,
+                                int out_dtype, const int64_t* rows,
+                                const int64_t* cols, int64_t count,
+                                double* ref, uint16_t* out);
+
+/* Contiguous grouped form.  a (m,k), b (G,n,k), a_scale (m,k/128) and
+ * b_scale (G,n/128,k/128), all K-major; m_indices (m) with -1 for padding.
+ * Rows with m_indices == -1 are not computed: written[i] = 0 there and 1
+ * elsewhere (written may be NULL), and ref/out rows are left untouched. */
+int oracle_group_gemm_contiguous(const uint8_t* a, const uint8_t* b,
+                                 const float* a_scale, const float* b_scale,
+                                 const int32_t* m_indices, int64_t m, int64_t n,
+                                 int64_t k, int64_t num_groups, double* ref,
+                                 uint16_t* out, uint8_t* written);
+
+/* Grouped form at chosen positions; a position on a padding row gets
+ * written[s] = 0 and is left untouched. */
+int oracle_group_gemm_contiguous_at(const uint8_t* a, const uint8_t* b,
+                                    const float* a_scale, const float* b_scale,
+                                    const int32_t* m_indices, int64_t m,
+                                    int64_t n, int64_t k, int64_t num_groups,
+                                    const int64_t* rows, const int64_t* cols,
+                                    int64_t count, double* ref, uint16_t* out,
+                                    uint8_t* written);
+
+/* Masked batched form.  a (G,max_m,k), b (G,n,k), a_scale (G,max_m,k/128),
+ * b_scale (G,n/128,k/128); masked_m (G).  Row r of group g is computed when
+ * r < clamp(masked_m[g], 0, max_m); other rows are left untouched and get
+ * written = 0.  Indices into ref/out/written are g*max_m*n + r*n + j. */
+int oracle_batch_gemm_masked(const uint8_t* a, const uint8_t* b,
+                             const float* a_scale, const float* b_scale,
+                             const int32_t* masked_m, int64_t num_groups,
+                             int64_t max_m, int64_t n, int64_t k, double* ref,
+                             uint16_t* out, uint8_t* written);
+
+/* Masked form at chosen positions: groups[s], rows[s] (row within the group)
+ * and cols[s]. */
+int oracle_batch_gemm_masked_at(const uint8_t* a, const uint8_t* b,
+                                const float* a_scale, const float* b_scale,
+                                const int32_t* masked_m, int64_t num_groups,
+                                int64_t max_m, int64_t n, int64_t k,
+                                const int64_t* groups, const int64_t* rows,
+                                const int64_t* cols, int64_t count, double* ref,
+                                uint16_t* out, uint8_t* written);
+
+/* Number of threads the oracle's parallel loops use. */
+int oracle_num_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

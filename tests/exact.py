@@ -1,0 +1,101 @@
+"""Exact rational restatement of the groupwise FP8 GEMM, for tiny shapes.
+
+An independent second implementation used to pin the C oracle: E4M3 decoded
+from its bit fields into ``fractions.Fraction``, block sums in Python integers
+(every E4M3 value is an integer multiple of 2^-9), scales converted exactly
+from FP32, and the final value rounded to BF16/FP16 by exact comparison.  It
+follows the MATE page "FlashInfer Wrapper APIs", section GEMM
+(gemm_fp8_nt_groupwise and its grouped and masked forms).
+"""
+from fractions import Fraction
+
+import numpy as np
+
+FORMATS = {
+    # significand bits (with the implicit one), smallest normal exponent,
+    # largest finite value
+    "bf16": (8, -126, Fraction(2 ** 8 - 1, 2 ** 7) * Fraction(2) ** 127),
+    "f16": (11, -14, Fraction(65504)),
+}
+
+
+def e4m3_value(code):
+    """Exact value of an E4M3 (float8_e4m3fn) code, None for NaN."""
+    s, e, f = (code >> 7) & 1, (code >> 3) & 0xF, code & 7
+    if e == 0xF and f == 7:
+        return None
+    if e == 0:
+        v = Fraction(f, 8) * Fraction(1, 2 ** 6)
+    else:
+        v = (1 + Fraction(f, 8)) * Fraction(2) ** (e - 7)
+    return -v if s else v
+
+
+def e4m3_units(code):
+    """The code's value in units of 2^-9 (an integer)."""
+    v = e4m3_value(code) * 512
+    assert v.denominator == 1
+    return int(v)
+
+
+UNITS = np.array([e4m3_units(c) if e4m3_value(c) is not None else 0
+                  for c in range(256)], dtype=np.int64)
+
+
+def floor_log2(x):
+    """floor(log2(x)) of a positive Fraction, exactly."""
+    e = x.numerator.bit_length() - x.denominator.bit_length()
+    while Fraction(2) ** e > x:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= x:
+        e += 1
+    return e
+
+
+def round_exact(x, fmt):
+    """Nearest value of format `fmt` to the Fraction x, ties to even.
+
+    Returns a Fraction, or +-inf (float) on overflow.
+    """
+    p, emin, maxf = FORMATS[fmt]
+    if x == 0:
+        return Fraction(0)
+    lead = max(floor_log2(abs(x)), emin)
+    quantum = Fraction(2) ** (lead - p + 1)
+    y = round(x / quantum) * quantum  # Fraction.__round__ ties to even
+    if abs(y) > maxf:
+        return float("inf") if x > 0 else float("-inf")
+    return y
+
+
+def block_sums(a_codes, b_codes):
+    """Integer block sums P*2^18, shape (rows_a, rows_b, k/128)."""
+    a = UNITS[np.asarray(a_codes, dtype=np.int64)]
+    b = UNITS[np.asarray(b_codes, dtype=np.int64)]
+    kb = a.shape[1] // 128
+    out = np.empty((a.shape[0], b.shape[0], kb), dtype=object)
+    for t in range(kb):
+        blk = a[:, t * 128:(t + 1) * 128] @ b[:, t * 128:(t + 1) * 128].T
+        out[:, :, t] = blk.astype(object)
+    return out
+
+
+def dense(a_codes, b_codes, sa, sb, with_abs=False):
+    """Exact R(i,j) for K-major scales sa (m,KB), sb (n/128,KB) (FP32 arrays).
+
+    With `with_abs`, also the sums of |P * sa * sb| over K blocks (the scale of
+    the rounding error an FP64 evaluation may make)."""
+    P = block_sums(a_codes, b_codes)
+    m, n, kb = P.shape
+    unit = Fraction(1, 2 ** 18)
+    sa = [[Fraction(float(v)) for v in row] for row in np.asarray(sa, np.float32)]
+    sb = [[Fraction(float(v)) for v in row] for row in np.asarray(sb, np.float32)]
+    R = [[None] * n for _ in range(m)]
+    A = [[None] * n for _ in range(m)]
+    for i in range(m):
+        for j in range(n):
+            jb = j // 128
+            terms = [int(P[i, j, t]) * unit * sa[i][t] * sb[jb][t] for t in range(kb)]
+            R[i][j] = sum(terms, Fraction(0))
+            A[i][j] = sum((abs(x) for x in terms), Fraction(0))
+    return (R, A) if with_abs else R

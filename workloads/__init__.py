@@ -1,0 +1,178 @@
+"""Seeded synthetic inputs for the FP8 groupwise-scaled NT GEMM.
+
+This module only draws random numbers and packs them into the operand layouts
+of the MATE page "FlashInfer Wrapper APIs", section GEMM; it holds none of the
+GEMM's arithmetic.  Both the CUDA path and the CPU oracle are fed the same
+tensors from here, so the oracle never sees anything the CUDA path produced.
+
+E4M3 codes come from torch's ``float8_e4m3fn`` cast (round to nearest even)
+after clipping to the format's finite range [-448, 448], so nothing saturates
+to NaN.  Scales are ``2**U(lo, hi)`` in FP32 (log-uniform).
+
+Random streams: a ``torch.Generator`` seeded with the given seed on the device
+the tensors are drawn on.  CPU and CUDA generators give different streams, so a
+workload is identified by (seed, device); every check compares the two
+implementations on the very same tensors.
+"""
+import math
+
+import torch
+
+E4M3_MAX = 448.0
+KBLOCK = 128  # scale granularity along k
+NBLOCK = 128  # scale granularity along n
+
+# The five synthetic workloads, by name.
+CONFIGS = {
+    "dense_128x256x256": dict(kind="dense", m=128, n=256, k=256, dist="uniform4",
+                              scale_exp=(-4.0, 2.0), out_dtype="bf16", seed=1001),
+    "dense_4096x7168x2048": dict(kind="dense", m=4096, n=7168, k=2048, dist="normal",
+                                 scale_exp=(-6.0, 0.0), out_dtype="bf16", seed=1002),
+    "grouped_4096tok_top8_e64_n4096_k7168": dict(
+        kind="grouped", num_tokens=4096, top_k=8, num_experts=64, n=4096, k=7168,
+        scale_exp=(-6.0, 0.0), seed=1003),
+    "masked_g32_maxm256_n4096_k7168": dict(
+        kind="masked", num_groups=32, max_m=256, n=4096, k=7168, expected_m=128,
+        scale_exp=(-6.0, 0.0), seed=1004),
+    "dense_16384x18432x7168": dict(kind="dense", m=16384, n=18432, k=7168, dist="normal",
+                                   scale_exp=(-6.0, 0.0), out_dtype="f16", seed=1005),
+}
+
+
+def generator(seed, device="cpu"):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def to_e4m3_codes(x):
+    """E4M3 codes (uint8) of float values: clip to +-448, cast RNE."""
+    x = x.float().clamp_(-E4M3_MAX, E4M3_MAX)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def _draw(shape, dist, gen, device, chunk_rows=None):
+    """E4M3 codes of `shape`, drawn row-chunk by row-chunk to bound memory."""
+    out = torch.empty(shape, dtype=torch.uint8, device=device)
+    flat = out.view(-1, shape[-1])
+    rows = flat.shape[0]
+    step = chunk_rows or max(1, (1 << 24) // max(1, shape[-1]))
+    for r0 in range(0, rows, step):
+        r1 = min(rows, r0 + step)
+        v = torch.empty((r1 - r0, shape[-1]), dtype=torch.float32, device=device)
+        if dist == "normal":
+            v.normal_(0.0, 1.0, generator=gen)
+        elif dist == "uniform4":
+            v.uniform_(-1.0, 1.0, generator=gen).mul_(4.0)
+        else:
+            raise ValueError(dist)
+        flat[r0:r1] = to_e4m3_codes(v)
+    return out
+
+
+def log_uniform(shape, lo, hi, gen, device="cpu"):
+    """FP32 values 2**U(lo, hi)."""
+    u = torch.empty(shape, dtype=torch.float32, device=device)
+    u.uniform_(lo, hi, generator=gen)
+    return torch.exp2(u)
+
+
+def dense(m, n, k, seed, dist="normal", scale_exp=(-6.0, 0.0), scale_major="K",
+          device="cpu", **_):
+    """a (m,k), b (n,k) E4M3 codes; scales in the requested layout."""
+    gen = generator(seed, device)
+    kb, nb = k // KBLOCK, n // NBLOCK
+    a = _draw((m, k), dist, gen, device)
+    b = _draw((n, k), dist, gen, device)
+    sa = log_uniform((m, kb), scale_exp[0], scale_exp[1], gen, device)
+    sb = log_uniform((nb, kb), scale_exp[0], scale_exp[1], gen, device)
+    if scale_major == "MN":
+        sa, sb = sa.t().contiguous(), sb.t().contiguous()
+    elif scale_major != "K":
+        raise ValueError(scale_major)
+    return dict(a=a, b=b, a_scale=sa, b_scale=sb, m=m, n=n, k=k,
+                scale_major=scale_major)
+
+
+def routing_m_indices(num_tokens, top_k, num_experts, gen, align=128):
+    """m_indices of the contiguous grouped layout for a top-k routing.
+
+    Each token picks `top_k` distinct experts uniformly at random (multinomial
+    without replacement).  Rows are grouped by expert in ascending order and
+    each expert's segment is padded with -1 up to a multiple of `align` rows.
+    """
+    w = torch.ones((num_tokens, num_experts), dtype=torch.float32)
+    choice = torch.multinomial(w, top_k, replacement=False, generator=gen)
+    counts = torch.bincount(choice.flatten(), minlength=num_experts).tolist()
+    parts = []
+    for e, c in enumerate(counts):
+        if c == 0:
+            continue
+        padded = int(math.ceil(c / align) * align)
+        seg = torch.full((padded,), -1, dtype=torch.int32)
+        seg[:c] = e
+        parts.append(seg)
+    if not parts:
+        return torch.empty(0, dtype=torch.int32)
+    return torch.cat(parts)
+
+
+def grouped(num_tokens, top_k, num_experts, n, k, seed, scale_exp=(-6.0, 0.0),
+            device="cpu", m_indices=None, **_):
+    """Contiguous grouped MoE operands; padding rows of a hold random data too."""
+    cpu_gen = generator(seed, "cpu")
+    mi = m_indices if m_indices is not None else routing_m_indices(
+        num_tokens, top_k, num_experts, cpu_gen)
+    mi = mi.to(torch.int32)
+    gen = generator(seed + 7919, device)
+    m = mi.numel()
+    kb, nb = k // KBLOCK, n // NBLOCK
+    a = _draw((m, k), "normal", gen, device)
+    b = _draw((num_experts, n, k), "normal", gen, device)
+    sa = log_uniform((m, kb), scale_exp[0], scale_exp[1], gen, device)
+    sb = log_uniform((num_experts, nb, kb), scale_exp[0], scale_exp[1], gen, device)
+    return dict(a=a, b=b, a_scale=sa, b_scale=sb, m_indices=mi.to(device), m=m, n=n,
+                k=k, num_groups=num_experts)
+
+
+def masked(num_groups, max_m, n, k, seed, scale_exp=(-6.0, 0.0), expected_m=None,
+           device="cpu", masked_m=None, **_):
+    """Masked batched MoE operands; masked_m ~ U{0..max_m} unless given."""
+    cpu_gen = generator(seed, "cpu")
+    mm = masked_m if masked_m is not None else torch.randint(
+        0, max_m + 1, (num_groups,), generator=cpu_gen, dtype=torch.int64)
+    mm = mm.to(torch.int32)
+    gen = generator(seed + 7919, device)
+    kb, nb = k // KBLOCK, n // NBLOCK
+    a = _draw((num_groups, max_m, k), "normal", gen, device)
+    b = _draw((num_groups, n, k), "normal", gen, device)
+    sa = log_uniform((num_groups, max_m, kb), scale_exp[0], scale_exp[1], gen, device)
+    sb = log_uniform((num_groups, nb, kb), scale_exp[0], scale_exp[1], gen, device)
+    return dict(a=a, b=b, a_scale=sa, b_scale=sb, masked_m=mm.to(device),
+                num_groups=num_groups, max_m=max_m, n=n, k=k,
+                expected_m=expected_m if expected_m is not None else max_m // 2)
+
+
+def make(name, device="cpu", **overrides):
+    """Operands of one of the named workloads."""
+    cfg = dict(CONFIGS[name])
+    cfg.update(overrides)
+    kind = cfg.pop("kind")
+    if kind == "dense":
+        return dense(device=device, **cfg)
+    if kind == "grouped":
+        return grouped(device=device, **cfg)
+    if kind == "masked":
+        return masked(device=device, **cfg)
+    raise ValueError(kind)
+
+
+def sample_positions(rows, cols, count, seed, extra_rows=()):
+    """`count` seeded (row, col) positions plus every column of `extra_rows`."""
+    gen = generator(seed, "cpu")
+    r = torch.randint(0, rows, (count,), generator=gen, dtype=torch.int64)
+    c = torch.randint(0, cols, (count,), generator=gen, dtype=torch.int64)
+    for er in extra_rows:
+        r = torch.cat([r, torch.full((cols,), int(er), dtype=torch.int64)])
+        c = torch.cat([c, torch.arange(cols, dtype=torch.int64)])
+    return r, c
