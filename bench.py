@@ -1,0 +1,533 @@
+#!/usr/bin/env python
+"""Throughput of the FP8 (E4M3) groupwise-scaled NT GEMM on GB300.
+
+One step = one pass of the whole hot path over one batch of the workload.  The
+default workload is the dense GEMM m=4096, n=7168, k=2048 with BF16 output, run
+once with K-major and once with MN-major scales: a step is those two calls.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  `value` is device-timed TFLOP/s over the K
+timed steps (CUDA events on the launching stream, inputs resident in HBM,
+input sets rotated so that the working set exceeds L2).  `e2e` is the same
+metric through the C ABI with host buffers: every step copies its inputs from
+pinned host memory and its output back.  The reference arm (`--impl
+reference`) is the CPU oracle timed on the host cores on a bounded sample.
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+(the GEMM has no exchange step); `value` is the work of all ranks divided by
+the slowest rank's time.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP8 groupwise GEMM TFLOP/s (device-timed) and % of GB300 dense FP8 roofline"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "dense_4096x7168x2048"
+L2_BYTES = 129 * 1024 * 1024
+FP8_OVER_BF16_NOMINAL = 4.5 / 2.25  # nominal dense FP8 / BF16 tensor rate
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- helpers
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def fp8_peak_tflops(peaks, sustained=False):
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    return peaks.get(key, peaks["bf16_tflops"]) * FP8_OVER_BF16_NOMINAL
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_block_scaled_nt_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel as it is now (same source hash) and on this workload."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel, {}).get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the GPU is busy."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap,utilization.gpu")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_id), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        samples = []
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                samples.append(dict(sm=float(parts[0]), sm_max=float(parts[1]),
+                                    power=float(parts[2]),
+                                    reasons=[r for r, v in zip(self.REASONS, parts[3:7])
+                                             if v.lower() == "active"],
+                                    util=float(parts[7])))
+            except ValueError:
+                continue
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        busy = [s for s in samples if s["util"] > 0] or samples
+        reasons = sorted({r for s in busy for r in s["reasons"]})
+        return {"sm_mhz": statistics.median(s["sm"] for s in busy),
+                "sm_max_mhz": max(s["sm_max"] for s in samples),
+                "power_w_max": max(s["power"] for s in busy),
+                "reasons": reasons, "samples": len(busy)}
+
+
+# --------------------------------------------------------------- workloads
+
+def workload_stats(name, w):
+    """Algorithmic FLOPs and bytes of one call (valid rows only)."""
+    import workloads
+    cfg = workloads.CONFIGS[name]
+    kind = cfg["kind"]
+    k = w["k"]
+    n = w["n"]
+    kb, nb = k // 128, n // 128
+    if kind == "dense":
+        m = w["m"]
+        out_b = 2
+        flops = 2.0 * m * n * k
+        bytes_ = m * k + n * k + 4 * (m * kb + nb * kb) + out_b * m * n
+        return flops, bytes_, "tensor"
+    if kind == "grouped":
+        mi = w["m_indices"].cpu()
+        valid = int((mi != -1).sum())
+        live = int(torch_unique_count(mi[mi != -1]))
+        flops = 2.0 * valid * n * k
+        bytes_ = live * n * k + valid * k + 2 * valid * n + 4 * (valid * kb + live * nb * kb)
+        return flops, bytes_, "tensor"
+    mm = w["masked_m"].cpu().clamp(0, w["max_m"])
+    s = int(mm.sum())
+    live = int((mm > 0).sum())
+    flops = 2.0 * s * n * k
+    bytes_ = live * n * k + s * k + 2 * s * n + 4 * (s * kb + live * nb * kb)
+    return flops, bytes_, "hbm"
+
+
+def torch_unique_count(t):
+    import torch
+    return torch.unique(t).numel()
+
+
+def make_sets(name, device):
+    """Input sets on the device, rotated step by step so that the bytes touched
+    between two uses of a set exceed L2.  Returns (sets, calls_per_step)."""
+    import torch
+    import workloads
+    cfg = workloads.CONFIGS[name]
+    if cfg["kind"] == "dense":
+        layouts = ("K", "MN") if name == DEFAULT_WORKLOAD else ("K",)
+    else:
+        layouts = (None,)
+    sets = []
+    per_set = 0
+    for s in range(8):
+        one = []
+        for li, major in enumerate(layouts):
+            seed = cfg["seed"] + 100 * s + li
+            if cfg["kind"] == "dense":
+                w = workloads.make(name, device=device, seed=seed, scale_major=major)
+                odt = torch.float16 if cfg["out_dtype"] == "f16" else torch.bfloat16
+                w["out"] = torch.empty((w["m"], w["n"]), dtype=odt, device=device)
+            elif cfg["kind"] == "grouped":
+                w = workloads.make(name, device=device, seed=seed)
+                w["out"] = torch.empty((w["m"], w["n"]), dtype=torch.bfloat16, device=device)
+            else:
+                w = workloads.make(name, device=device, seed=seed)
+                w["out"] = torch.empty((w["num_groups"], w["max_m"], w["n"]),
+                                       dtype=torch.bfloat16, device=device)
+            per_set += sum(v.numel() * v.element_size() for v in w.values()
+                           if torch.is_tensor(v))
+            one.append(w)
+        sets.append(one)
+        if per_set >= 3 * L2_BYTES:
+            break
+    return sets, len(layouts)
+
+
+def call_args(lib, name, w, stream_handle):
+    """ctypes argument tuple of the C entry point for one call."""
+    import workloads
+    kind = workloads.CONFIGS[name]["kind"]
+    p = lambda t: t.data_ptr()  # noqa: E731
+    if kind == "dense":
+        import torch
+        od = 1 if w["out"].dtype == torch.float16 else 0
+        sm = 1 if w["scale_major"] == "MN" else 0
+        return (lib.fp8_gemm_nt_groupwise,
+                (p(w["a"]), p(w["b"]), p(w["a_scale"]), p(w["b_scale"]), p(w["out"]), od,
+                 w["m"], w["n"], w["k"], sm, 1, 128, 128, 1, stream_handle))
+    if kind == "grouped":
+        return (lib.fp8_group_gemm_contiguous,
+                (p(w["a"]), p(w["b"]), p(w["a_scale"]), p(w["b_scale"]), p(w["m_indices"]),
+                 p(w["out"]), w["m"], w["n"], w["k"], w["num_groups"], stream_handle))
+    return (lib.fp8_batch_gemm_masked,
+            (p(w["a"]), p(w["b"]), p(w["a_scale"]), p(w["b_scale"]), p(w["masked_m"]),
+             w["expected_m"], p(w["out"]), w["num_groups"], w["max_m"], w["n"], w["k"],
+             stream_handle))
+
+
+# ------------------------------------------------------------ oracle timing
+
+def oracle_sample_rate(name, w, seconds, seed=21):
+    """Time the oracle on a bounded sample of output elements of one call.
+    Returns (flops_per_second, samples, seconds_taken, threads, positions, ref)."""
+    import numpy as np
+    import oracle
+    import workloads
+    cfg = workloads.CONFIGS[name]
+    host = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in w.items() if k != "out"}
+
+    def run(count):
+        g = np.random.default_rng(seed)
+        if cfg["kind"] == "dense":
+            r = g.integers(0, host["m"], count)
+            c = g.integers(0, host["n"], count)
+            sm = oracle.SCALE_MN_MAJOR if host["scale_major"] == "MN" else oracle.SCALE_K_MAJOR
+            od = oracle.OUT_F16 if cfg["out_dtype"] == "f16" else oracle.OUT_BF16
+            t0 = time.perf_counter()
+            ref, _ = oracle.gemm_nt_groupwise_at(host["a"], host["b"], host["a_scale"],
+                                                 host["b_scale"], r, c, sm, od)
+            dt = time.perf_counter() - t0
+            return dt, (r, c), ref, np.ones(count, bool)
+        if cfg["kind"] == "grouped":
+            mi = host["m_indices"].numpy()
+            valid_rows = np.nonzero(mi != -1)[0]
+            r = valid_rows[g.integers(0, valid_rows.size, count)]
+            c = g.integers(0, host["n"], count)
+            t0 = time.perf_counter()
+            ref, _, wr = oracle.group_gemm_contiguous_at(host["a"], host["b"], host["a_scale"],
+                                                         host["b_scale"], host["m_indices"], r, c)
+            return time.perf_counter() - t0, (r, c), ref, wr
+        mm = host["masked_m"].numpy().clip(0, host["max_m"])
+        groups = np.nonzero(mm > 0)[0]
+        gs = groups[g.integers(0, groups.size, count)]
+        rs = (g.random(count) * mm[gs]).astype(np.int64)
+        cs = g.integers(0, host["n"], count)
+        t0 = time.perf_counter()
+        ref, _, wr = oracle.batch_gemm_masked_at(host["a"], host["b"], host["a_scale"],
+                                                 host["b_scale"], host["masked_m"], gs, rs, cs)
+        return time.perf_counter() - t0, (gs, rs, cs), ref, wr
+
+    probe = 1024
+    dt, _, _, _ = run(probe)
+    count = int(max(probe, min(50_000_000, probe * seconds / max(dt, 1e-6))))
+    dt, pos, ref, wr = run(count)
+    flops = 2.0 * host["k"] * int(wr.sum())
+    return flops / dt, count, dt, oracle.num_threads(), pos, ref, wr
+
+
+# ------------------------------------------------------------------ arms
+
+def run_reference(args):
+    """CPU oracle arm: each step is the oracle on a bounded sample of the workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import workloads
+    w = workloads.make(args.workload, device="cpu")
+    total = args.steps + args.warmup
+    per_step = max(0.05, min(5.0, 150.0 / max(total, 1)))
+    # one calibration run sizes the sample so that a step takes about per_step
+    rate, count, dt, threads, _, _, _ = oracle_sample_rate(args.workload, w, per_step)
+    times = []
+    flops = 0.0
+    for i in range(total):
+        r, c_, d, th, _, _, wr = oracle_sample_rate(args.workload, w, per_step, seed=100 + i)
+        if i >= args.warmup:
+            times.append(d)
+            flops += r * d
+    elapsed = sum(times)
+    value = flops / elapsed / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * elapsed / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "%d seeded output elements per step of %s (each the full "
+                                   "k-long FP64 dot product and scale promotion)"
+                                   % (count, args.workload)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import fp8_block_scaled_nt_gb300 as fp8g
+    from fp8_block_scaled_nt_gb300 import _build
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    _build.build()
+    lib = fp8g.load()
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    sets, calls_per_step = make_sets(args.workload, dev)
+    flops_call, bytes_call, bound = workload_stats(args.workload, sets[0][0])
+    flops_step = flops_call * calls_per_step
+    calls = [[call_args(lib, args.workload, w, sh) for w in one] for one in sets]
+
+    def step(i):
+        for fn, a in calls[i % len(calls)]:
+            rc = fn(*a)
+            if rc != 0:
+                raise fp8g.Fp8gError(rc, fn.__name__, fp8g.last_error())
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else str(local_rank)
+    sampler = ClockSampler(gpu_id)
+    # settle clocks (untimed, >= 1 s of back-to-back steps), then warm up
+    t_end = time.time() + 1.0
+    i = 0
+    while time.time() < t_end:
+        step(i)
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize(dev)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    fp8g.get_device_status(clear=True)
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    region_ms = ev0.elapsed_time(ev1)
+    clocks = sampler.stop()
+    status = fp8g.get_device_status(clear=True)
+    if status:
+        raise RuntimeError("device status %#x after the timed region" % status)
+
+    if world > 1:
+        t = torch.tensor([region_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        region_ms = float(t.item())
+
+    # End to end through the C ABI with host buffers: per step, copy the inputs
+    # of every call from pinned host memory, run the calls, copy outputs back.
+    host_sets = []
+    for one in sets[:1]:
+        hs = []
+        for w in one:
+            hs.append({k: v.cpu().pin_memory() for k, v in w.items() if torch.is_tensor(v)})
+        host_sets.append(hs)
+    h2d = sum(v.numel() * v.element_size() for hs in host_sets[0] for k, v in hs.items()
+              if k != "out")
+    d2h = sum(hs["out"].numel() * hs["out"].element_size() for hs in host_sets[0])
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        for w, hs in zip(sets[0], host_sets[0]):
+            for k, v in hs.items():
+                if k != "out":
+                    w[k].copy_(v, non_blocking=True)
+        for fn, a in calls[0]:
+            rc = fn(*a)
+            if rc != 0:
+                raise fp8g.Fp8gError(rc, fn.__name__, fp8g.last_error())
+        for w, hs in zip(sets[0], host_sets[0]):
+            hs["out"].copy_(w["out"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_value = flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_value = world * flops_step * e2e_steps / (float(t.item()) * 1e-3) / 1e12
+
+    value = world * flops_step * args.steps / (region_ms * 1e-3) / 1e12
+    launches = args.steps * calls_per_step
+    avg_launch_s = region_ms * 1e-3 / launches
+    peaks, peaks_src = load_peaks()
+    kernel_name = {"dense": "gemm_kernel<dense>", "grouped": "gemm_kernel<grouped>",
+                   "masked": "gemm_kernel<masked>"}[workload_kind(args.workload)]
+    if bound == "tensor":
+        achieved = flops_call / avg_launch_s / 1e12
+        peak = fp8_peak_tflops(peaks)
+        unit = "TFLOP/s"
+    else:
+        achieved = bytes_call / avg_launch_s / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": dram_traffic(kernel_name, args.workload),
+                "peak_source": "%s (%s)" % (peaks_src, "bf16 burst x 2 nominal fp8/bf16 ratio"
+                                            if bound == "tensor" else "hbm copy"),
+                "kernel": kernel_name, "algorithmic_flops_per_launch": flops_call,
+                "algorithmic_bytes_per_launch": bytes_call,
+                "avg_launch_us": avg_launch_s * 1e6}
+
+    cpu_baseline = None
+    spot = None
+    if rank == 0 and not args.no_cpu_baseline:
+        w0 = sets[0][0]
+        rate, count, dt, threads, pos, ref, wr = oracle_sample_rate(args.workload, w0,
+                                                                    args.cpu_seconds)
+        cpu_baseline = {"value": rate / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+                        "sample": "%d seeded output elements of one %s call (%.1f s)"
+                                  % (count, args.workload, dt)}
+        # spot check of the benchmarked kernel's output at the oracle's positions
+        # (set 0 was last written by the end-to-end loop from the same inputs)
+        torch.cuda.synchronize(dev)
+        got = w0["out"].float().cpu().double().numpy()[tuple(pos)]
+        ref = np.asarray(ref)
+        rms = float(np.sqrt(np.mean(ref[wr] ** 2)))
+        ok = bool(np.all(np.abs(got[wr] - ref[wr]) <= 1e-2 * np.abs(ref[wr]) + 2e-3 * rms))
+        spot = {"elements": int(wr.sum()), "within_tolerance": ok}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": region_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
+            "data": "synthetic",
+            "config": config_block(args.workload, sets, calls_per_step, world),
+            "roofline": roofline, "cpu_baseline": cpu_baseline,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": launches, "clocks": clocks, "spot_check": spot,
+            "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def workload_kind(name):
+    import workloads
+    return workloads.CONFIGS[name]["kind"]
+
+
+def config_block(name, sets, calls_per_step, world):
+    import workloads
+    cfg = dict(workloads.CONFIGS[name])
+    block = {"workload": name, "calls_per_step": calls_per_step,
+             "l2": "inputs larger than L2: %d input sets rotated per step" % len(sets),
+             "parallelism": "replicas" if world > 1 else "single"}
+    block.update({k: v for k, v in cfg.items() if k not in ("kind",)})
+    if name == DEFAULT_WORKLOAD:
+        block["scale_layouts"] = ["K", "MN"]
+    return block
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

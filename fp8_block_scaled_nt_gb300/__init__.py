@@ -1,0 +1,275 @@
+"""FP8 (E4M3) groupwise-scaled NT GEMM for GB300 (sm_103a).
+
+Thin Python binding of the C ABI in ``include/fp8g.h``.  It only marshals
+arguments — tensor pointers, sizes, the current CUDA stream — and raises on a
+non-zero status; every step of the computation runs in the library's CUDA
+kernels.  If ``libfp8g.so`` is missing, calls fail: there is no other path.
+
+Two layers, both following the MATE page "FlashInfer Wrapper APIs", section
+GEMM:
+
+* ``fp8_gemm_nt_groupwise``, ``fp8_group_gemm_contiguous``,
+  ``fp8_batch_gemm_masked`` — the C entry points, same names, taking tensors
+  and a preallocated ``out``;
+* ``gemm_fp8_nt_groupwise``, ``group_deepgemm_fp8_nt_groupwise``,
+  ``batch_deepgemm_fp8_nt_groupwise`` — the page's own signatures, which
+  allocate ``out`` when it is omitted and return it.
+
+E4M3 operands may be ``torch.float8_e4m3fn`` or ``torch.uint8`` (raw codes).
+"""
+import ctypes
+import os
+
+__all__ = [
+    "Fp8gError", "load", "last_error", "get_device_status",
+    "fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
+    "gemm_fp8_nt_groupwise", "group_deepgemm_fp8_nt_groupwise",
+    "batch_deepgemm_fp8_nt_groupwise",
+    "OK", "ERR_INVALID_ARGUMENT", "ERR_UNSUPPORTED", "ERR_ARCH", "ERR_CUDA", "ERR_TIMEOUT",
+    "DEVICE_TIMEOUT", "DEVICE_BAD_M_INDICES", "DEVICE_MASKED_M_CLAMPED",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp8g.so")
+
+OK, ERR_INVALID_ARGUMENT, ERR_UNSUPPORTED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(6)
+STATUS_NAMES = {0: "FP8G_OK", 1: "FP8G_ERR_INVALID_ARGUMENT", 2: "FP8G_ERR_UNSUPPORTED",
+                3: "FP8G_ERR_ARCH", 4: "FP8G_ERR_CUDA", 5: "FP8G_ERR_TIMEOUT"}
+SCALE_K_MAJOR, SCALE_MN_MAJOR = 0, 1
+OUT_BF16, OUT_F16 = 0, 1
+DEVICE_TIMEOUT, DEVICE_BAD_M_INDICES, DEVICE_MASKED_M_CLAMPED = 0x1, 0x2, 0x4
+
+
+class Fp8gError(RuntimeError):
+    def __init__(self, status, func, message):
+        super().__init__("%s: %s: %s" % (func, STATUS_NAMES.get(status, status), message))
+        self.status = status
+
+
+_lib = None
+
+
+def load():
+    """Load ``libfp8g.so`` (built by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("fp8g CUDA library not built (%s missing); run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.fp8_gemm_nt_groupwise.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, I, I, I, I, P]
+    lib.fp8_group_gemm_contiguous.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, P]
+    lib.fp8_batch_gemm_masked.argtypes = [P, P, P, P, P, I64, P, I64, I64, I64, I64, P]
+    lib.fp8g_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
+    for f in ("fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
+              "fp8g_get_device_status"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.fp8g_last_error.argtypes = []
+    lib.fp8g_last_error.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def last_error():
+    return load().fp8g_last_error().decode()
+
+
+def _raise_on(rc, func):
+    if rc != OK:
+        raise Fp8gError(rc, func, last_error())
+
+
+def get_device_status(clear=True):
+    """OR of DEVICE_* bits raised by kernels on the current device (synchronises)."""
+    v = ctypes.c_uint(0)
+    rc = load().fp8g_get_device_status(ctypes.byref(v), 1 if clear else 0)
+    if rc not in (OK, ERR_TIMEOUT):
+        _raise_on(rc, "fp8g_get_device_status")
+    return v.value
+
+
+# ------------------------------------------------------------- marshalling
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return t.data_ptr() if t is not None else None
+
+
+def _stream_handle(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+def _e4m3(t, name):
+    torch = _torch()
+    if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise TypeError("%s must be float8_e4m3fn (or uint8 codes), got %s" % (name, t.dtype))
+    return t
+
+
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda_contig(ts, names):
+    dev = None
+    for t, nm in zip(ts, names):
+        if t is None:
+            continue
+        _need(t.is_cuda, "%s must be a CUDA tensor" % nm)
+        _need(t.is_contiguous(), "%s must be contiguous" % nm)
+        if dev is None:
+            dev = t.device
+        _need(t.device == dev, "%s is on %s, expected %s" % (nm, t.device, dev))
+    return dev
+
+
+def _out_code(dtype):
+    torch = _torch()
+    if dtype == torch.bfloat16:
+        return OUT_BF16
+    if dtype == torch.float16:
+        return OUT_F16
+    raise TypeError("output dtype must be bfloat16 or float16, got %s" % dtype)
+
+
+def _check_granularity(g):
+    if tuple(g) != (1, 128, 128):
+        raise Fp8gError(ERR_UNSUPPORTED, "scale_granularity_mnk",
+                        "only (1, 128, 128) is provided, got %s" % (tuple(g),))
+
+
+# ------------------------------------------------------------- C entry points
+
+def fp8_gemm_nt_groupwise(a, b, a_scale, b_scale, out, scale_major="K", mma_sm=1,
+                          scale_granularity_mnk=(1, 128, 128), stream=None):
+    """out (m,n) = a (m,k) @ b (n,k).T with groupwise scales; returns out."""
+    torch = _torch()
+    _e4m3(a, "a"), _e4m3(b, "b")
+    _need(a.dim() == 2 and b.dim() == 2 and out.dim() == 2, "a, b, out must be 2-D")
+    m, k = a.shape
+    n = b.shape[0]
+    _need(b.shape[1] == k, "b must be (n, %d), got %s" % (k, tuple(b.shape)))
+    _need(tuple(out.shape) == (m, n), "out must be (%d, %d), got %s" % (m, n, tuple(out.shape)))
+    _need(a_scale.dtype == torch.float32 and b_scale.dtype == torch.float32, "scales must be float32")
+    kb, nb = k // 128, n // 128
+    if scale_major in (None, "K"):
+        sm = SCALE_K_MAJOR
+        _need(tuple(a_scale.shape) == (m, kb), "K-major a_scale must be (%d, %d)" % (m, kb))
+        _need(tuple(b_scale.shape) == (nb, kb), "K-major b_scale must be (%d, %d)" % (nb, kb))
+    elif scale_major == "MN":
+        sm = SCALE_MN_MAJOR
+        _need(tuple(a_scale.shape) == (kb, m), "MN-major a_scale must be (%d, %d)" % (kb, m))
+        _need(tuple(b_scale.shape) == (kb, nb), "MN-major b_scale must be (%d, %d)" % (kb, nb))
+    else:
+        raise ValueError("scale_major must be 'K', 'MN' or None")
+    dev = _cuda_contig((a, b, a_scale, b_scale, out), ("a", "b", "a_scale", "b_scale", "out"))
+    g = tuple(scale_granularity_mnk)
+    rc = load().fp8_gemm_nt_groupwise(
+        _ptr(a), _ptr(b), _ptr(a_scale), _ptr(b_scale), _ptr(out), _out_code(out.dtype),
+        m, n, k, sm, g[0], g[1], g[2], int(mma_sm), _stream_handle(stream, dev))
+    _raise_on(rc, "fp8_gemm_nt_groupwise")
+    return out
+
+
+def fp8_group_gemm_contiguous(a, b, a_scale, b_scale, m_indices, out, stream=None):
+    """out[i] = a[i] @ b[m_indices[i]].T for rows with m_indices != -1."""
+    torch = _torch()
+    _e4m3(a, "a"), _e4m3(b, "b")
+    _need(a.dim() == 2 and b.dim() == 3, "a must be (m, k) and b (num_groups, n, k)")
+    m, k = a.shape
+    g, n = b.shape[0], b.shape[1]
+    _need(b.shape[2] == k, "b must be (G, n, %d)" % k)
+    _need(tuple(out.shape) == (m, n) and out.dtype == torch.bfloat16, "out must be bf16 (m, n)")
+    _need(tuple(a_scale.shape) == (m, k // 128), "a_scale must be (m, k // 128)")
+    _need(tuple(b_scale.shape) == (g, n // 128, k // 128), "b_scale must be (G, n // 128, k // 128)")
+    _need(a_scale.dtype == torch.float32 and b_scale.dtype == torch.float32, "scales must be float32")
+    _need(m_indices.dtype == torch.int32 and tuple(m_indices.shape) == (m,),
+          "m_indices must be int32 (m,)")
+    dev = _cuda_contig((a, b, a_scale, b_scale, m_indices, out),
+                       ("a", "b", "a_scale", "b_scale", "m_indices", "out"))
+    rc = load().fp8_group_gemm_contiguous(
+        _ptr(a), _ptr(b), _ptr(a_scale), _ptr(b_scale), _ptr(m_indices), _ptr(out),
+        m, n, k, g, _stream_handle(stream, dev))
+    _raise_on(rc, "fp8_group_gemm_contiguous")
+    return out
+
+
+def fp8_batch_gemm_masked(a, b, a_scale, b_scale, masked_m, expected_m, out, stream=None):
+    """out[g, :masked_m[g]] = a[g, :masked_m[g]] @ b[g].T."""
+    torch = _torch()
+    _e4m3(a, "a"), _e4m3(b, "b")
+    _need(a.dim() == 3 and b.dim() == 3, "a must be (G, max_m, k) and b (G, n, k)")
+    g, max_m, k = a.shape
+    n = b.shape[1]
+    _need(b.shape[0] == g and b.shape[2] == k, "b must be (%d, n, %d)" % (g, k))
+    _need(tuple(out.shape) == (g, max_m, n) and out.dtype == torch.bfloat16,
+          "out must be bf16 (G, max_m, n)")
+    _need(tuple(a_scale.shape) == (g, max_m, k // 128), "a_scale must be (G, max_m, k // 128)")
+    _need(tuple(b_scale.shape) == (g, n // 128, k // 128), "b_scale must be (G, n // 128, k // 128)")
+    _need(a_scale.dtype == torch.float32 and b_scale.dtype == torch.float32, "scales must be float32")
+    _need(masked_m.dtype == torch.int32 and tuple(masked_m.shape) == (g,),
+          "masked_m must be int32 (G,)")
+    dev = _cuda_contig((a, b, a_scale, b_scale, masked_m, out),
+                       ("a", "b", "a_scale", "b_scale", "masked_m", "out"))
+    rc = load().fp8_batch_gemm_masked(
+        _ptr(a), _ptr(b), _ptr(a_scale), _ptr(b_scale), _ptr(masked_m), int(expected_m),
+        _ptr(out), g, max_m, n, k, _stream_handle(stream, dev))
+    _raise_on(rc, "fp8_batch_gemm_masked")
+    return out
+
+
+# ------------------------------------------------------------- page signatures
+
+def gemm_fp8_nt_groupwise(a, b, a_scale, b_scale, scale_major_mode=None, mma_sm=1,
+                          scale_granularity_mnk=(1, 128, 128), out=None, out_dtype=None,
+                          backend="auto", output_scale=None):
+    """The page's ``gemm_fp8_nt_groupwise``: returns out (m, n)."""
+    torch = _torch()
+    if output_scale is not None:
+        raise Fp8gError(ERR_UNSUPPORTED, "gemm_fp8_nt_groupwise",
+                        "FP8 output with output_scale is not provided")
+    if backend != "auto":
+        raise Fp8gError(ERR_UNSUPPORTED, "gemm_fp8_nt_groupwise",
+                        "only backend='auto' (this library's sm_103a kernel) exists")
+    _check_granularity(scale_granularity_mnk)
+    if out is None:
+        out = torch.empty((a.shape[0], b.shape[0]), device=a.device,
+                          dtype=out_dtype if out_dtype is not None else torch.bfloat16)
+    return fp8_gemm_nt_groupwise(a, b, a_scale, b_scale, out, scale_major_mode or "K", mma_sm,
+                                 scale_granularity_mnk)
+
+
+def group_deepgemm_fp8_nt_groupwise(a, b, a_scale, b_scale, m_indices,
+                                    scale_granularity_mnk=(1, 128, 128), out=None,
+                                    out_dtype=None):
+    """The page's ``group_deepgemm_fp8_nt_groupwise``: returns out (m, n) BF16."""
+    torch = _torch()
+    _check_granularity(scale_granularity_mnk)
+    if out is None:
+        if out_dtype not in (None, torch.bfloat16):
+            raise TypeError("only bfloat16 output is supported")
+        out = torch.empty((a.shape[0], b.shape[1]), device=a.device, dtype=torch.bfloat16)
+    return fp8_group_gemm_contiguous(a, b, a_scale, b_scale, m_indices, out)
+
+
+def batch_deepgemm_fp8_nt_groupwise(a, b, a_scale, b_scale, masked_m, expected_m,
+                                    scale_granularity_mnk=(1, 128, 128), out=None,
+                                    out_dtype=None):
+    """The page's ``batch_deepgemm_fp8_nt_groupwise``: returns out (G, max_m, n) BF16."""
+    torch = _torch()
+    _check_granularity(scale_granularity_mnk)
+    if out is None:
+        if out_dtype not in (None, torch.bfloat16):
+            raise TypeError("only bfloat16 output is supported")
+        out = torch.empty((a.shape[0], a.shape[1], b.shape[1]), device=a.device,
+                          dtype=torch.bfloat16)
+    return fp8_batch_gemm_masked(a, b, a_scale, b_scale, masked_m, expected_m, out)

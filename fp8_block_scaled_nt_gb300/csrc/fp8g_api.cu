@@ -1,0 +1,360 @@
+// C ABI of the FP8 groupwise-scaled NT GEMM: host-side validation, tensor-map
+// encoding and launch of the sm_103a kernel (gemm_kernel.cuh).
+//
+// The three entry points follow the MATE page "FlashInfer Wrapper APIs",
+// section GEMM (gemm_fp8_nt_groupwise, group_deepgemm_fp8_nt_groupwise,
+// batch_deepgemm_fp8_nt_groupwise).  The calling conventions — caller-owned
+// memory, enqueue on the caller's stream without synchronising, status code
+// plus a last-error message, nothing thrown across the boundary — follow the
+// "flashmla-rs" page, section Design Notes.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "fp8g.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+using fp8g::Params;
+
+__device__ unsigned int g_device_status;  // OR of FP8G_DEVICE_* bits, per device
+
+thread_local std::string t_last_error;
+
+fp8g_status_t fail(fp8g_status_t s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return s;
+}
+
+fp8g_status_t cuda_fail(cudaError_t e, const char* what) {
+    return fail(FP8G_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+constexpr int kNumKernels = 4;  // dense bf16, dense f16, grouped, masked
+
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    int cc_major = 0, cc_minor = 0;
+    int sm_count = 0;
+    unsigned int* status = nullptr;
+    bool smem_attr_set[kNumKernels] = {};
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Current device, checked to be sm_103 and set up once (status word address,
+// tensor-map encoder).
+fp8g_status_t device_state(DeviceState** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(FP8G_ERR_UNSUPPORTED, "device %d", dev);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& ds = g_devices[dev];
+    if (!ds.probed) {
+        cudaDeviceProp prop;
+        e = cudaGetDeviceProperties(&prop, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+        ds.cc_major = prop.major;
+        ds.cc_minor = prop.minor;
+        ds.sm_count = prop.multiProcessorCount;
+        ds.supported = prop.major == 10 && prop.minor == 3;
+        if (ds.supported) {
+            void* addr = nullptr;
+            e = cudaGetSymbolAddress(&addr, g_device_status);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+            ds.status = static_cast<unsigned int*>(addr);
+        }
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return fail(FP8G_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        ds.probed = true;
+    }
+    if (!ds.supported)
+        return fail(FP8G_ERR_ARCH, "device %d is sm_%d%d; this library needs sm_103 (GB300)", dev,
+                    ds.cc_major, ds.cc_minor);
+    *out = &ds;
+    return FP8G_OK;
+}
+
+// Row-major E4M3 matrix of `rows` x `k` bytes as a 2-D TMA view, tile
+// `box_rows` x 128 bytes, 128-byte swizzle; rows past the end read as zero.
+fp8g_status_t encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k,
+                         int box_rows, const char* what) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(k)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(fp8g::BLOCK_K), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t elem_strides[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                          strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FP8G_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what,
+                    static_cast<int>(r));
+    return FP8G_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+// Shape checks shared by all forms.
+fp8g_status_t check_nk(int64_t n, int64_t k) {
+    if (n <= 0 || n % 128)
+        return fail(FP8G_ERR_INVALID_ARGUMENT, "n = %lld must be a positive multiple of 128",
+                    (long long)n);
+    if (k <= 0 || k % 128)
+        return fail(FP8G_ERR_INVALID_ARGUMENT, "k = %lld must be a positive multiple of 128",
+                    (long long)k);
+    if (n > kMaxDim || k > kMaxDim)
+        return fail(FP8G_ERR_UNSUPPORTED, "n and k must be < 2^31");
+    return FP8G_OK;
+}
+
+// Pointer checks shared by all forms (non-empty problems only: an empty
+// tensor may have a null data pointer).
+fp8g_status_t check_ptrs(const void* a, const void* b, const float* a_scale, const float* b_scale,
+                         const void* out) {
+    if (!a || !b || !a_scale || !b_scale || !out)
+        return fail(FP8G_ERR_INVALID_ARGUMENT, "null pointer among a, b, a_scale, b_scale, out");
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(out, 16))
+        return fail(FP8G_ERR_INVALID_ARGUMENT, "a, b and out must be 16-byte aligned");
+    if (!aligned(a_scale, 4) || !aligned(b_scale, 4))
+        return fail(FP8G_ERR_INVALID_ARGUMENT, "scales must be 4-byte aligned");
+    return FP8G_OK;
+}
+
+template <int FORM, typename OutT>
+fp8g_status_t launch(DeviceState& ds, int slot, const CUtensorMap& map_a, const CUtensorMap& map_b,
+                     const Params& p, int64_t max_tiles, cudaStream_t stream) {
+    auto kernel = fp8g::gemm_kernel<FORM, OutT>;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!ds.smem_attr_set[slot]) {
+            // The kernel moves registers between its warpgroups (setmaxnreg); that
+            // is only safe if it is launched with exactly the budget it was built
+            // for, so check the compiled register count before the first launch.
+            cudaFuncAttributes attr;
+            cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
+            if (attr.numRegs != static_cast<int>(fp8g::LAUNCH_REGS))
+                return fail(FP8G_ERR_UNSUPPORTED,
+                            "kernel built with %d registers per thread, expected %u", attr.numRegs,
+                            fp8g::LAUNCH_REGS);
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(fp8g::SMEM_BYTES));
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+            ds.smem_attr_set[slot] = true;
+        }
+    }
+    const int grid = static_cast<int>(max_tiles < ds.sm_count ? max_tiles : ds.sm_count);
+    (void)cudaGetLastError();
+    kernel<<<grid, fp8g::NUM_THREADS, fp8g::SMEM_BYTES, stream>>>(map_a, map_b, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    t_last_error.clear();
+    return FP8G_OK;
+}
+
+Params base_params(const float* a_scale, const float* b_scale, void* out, int64_t rows, int64_t n,
+                   int64_t k) {
+    Params p{};
+    p.a_scale = a_scale;
+    p.b_scale = b_scale;
+    p.out = out;
+    p.rows = static_cast<int>(rows);
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.kblocks = static_cast<int>(k / 128);
+    p.nblocks = static_cast<int>(n / 128);
+    p.n_tiles = static_cast<int>((n + fp8g::BLOCK_N - 1) / fp8g::BLOCK_N);
+    p.m_blocks = static_cast<int>((rows + fp8g::BLOCK_M - 1) / fp8g::BLOCK_M);
+    p.band_m = 8;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fp8g_last_error(void) { return t_last_error.c_str(); }
+
+fp8g_status_t fp8_gemm_nt_groupwise(const void* a, const void* b, const float* a_scale,
+                                    const float* b_scale, void* out, fp8g_dtype_t out_dtype,
+                                    int64_t m, int64_t n, int64_t k, fp8g_scale_major_t scale_major,
+                                    int gran_m, int gran_n, int gran_k, int mma_sm,
+                                    cudaStream_t stream) {
+    try {
+        if (m < 0) return fail(FP8G_ERR_INVALID_ARGUMENT, "m = %lld < 0", (long long)m);
+        if (out_dtype != FP8G_OUT_BF16 && out_dtype != FP8G_OUT_F16)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "out_dtype %d is neither BF16 nor FP16",
+                        (int)out_dtype);
+        if (scale_major != FP8G_SCALE_K_MAJOR && scale_major != FP8G_SCALE_MN_MAJOR)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "scale_major %d is neither K nor MN",
+                        (int)scale_major);
+        if (mma_sm < 0 || mma_sm > 2)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "mma_sm = %d (expected 0, 1 or 2)", mma_sm);
+        if (gran_m != 1 || gran_n != 128 || gran_k != 128)
+            return fail(FP8G_ERR_UNSUPPORTED,
+                        "scale granularity (%d,%d,%d): only (1,128,128) is provided", gran_m,
+                        gran_n, gran_k);
+        if (m > kMaxDim) return fail(FP8G_ERR_UNSUPPORTED, "m must be < 2^31");
+        fp8g_status_t s = check_nk(n, k);
+        if (s != FP8G_OK) return s;
+        if (m == 0) {
+            t_last_error.clear();
+            return FP8G_OK;
+        }
+        if ((s = check_ptrs(a, b, a_scale, b_scale, out)) != FP8G_OK) return s;
+        const int64_t tiles = ((m + 127) / 128) * ((n + 255) / 256);
+        if (tiles > kMaxDim) return fail(FP8G_ERR_UNSUPPORTED, "problem has too many tiles");
+        DeviceState* ds = nullptr;
+        if ((s = device_state(&ds)) != FP8G_OK) return s;
+        CUtensorMap map_a, map_b;
+        if ((s = encode_map(&map_a, a, m, k, fp8g::BLOCK_M, "a")) != FP8G_OK) return s;
+        if ((s = encode_map(&map_b, b, n, k, fp8g::BLOCK_N, "b")) != FP8G_OK) return s;
+        Params p = base_params(a_scale, b_scale, out, m, n, k);
+        p.num_tiles = static_cast<int>(tiles);
+        p.num_groups = 1;
+        p.scale_mn_major = scale_major == FP8G_SCALE_MN_MAJOR;
+        p.status = ds->status;
+        if (out_dtype == FP8G_OUT_BF16)
+            return launch<fp8g::FORM_DENSE, __nv_bfloat16>(*ds, 0, map_a, map_b, p, tiles, stream);
+        return launch<fp8g::FORM_DENSE, __half>(*ds, 1, map_a, map_b, p, tiles, stream);
+    } catch (...) {
+        return fail(FP8G_ERR_CUDA, "unexpected exception");
+    }
+}
+
+fp8g_status_t fp8_group_gemm_contiguous(const void* a, const void* b, const float* a_scale,
+                                        const float* b_scale, const int32_t* m_indices, void* out,
+                                        int64_t m, int64_t n, int64_t k, int64_t num_groups,
+                                        cudaStream_t stream) {
+    try {
+        if (m < 0) return fail(FP8G_ERR_INVALID_ARGUMENT, "m = %lld < 0", (long long)m);
+        if (num_groups <= 0)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "num_groups = %lld must be >= 1",
+                        (long long)num_groups);
+        if (m > kMaxDim) return fail(FP8G_ERR_UNSUPPORTED, "m must be < 2^31");
+        fp8g_status_t s = check_nk(n, k);
+        if (s != FP8G_OK) return s;
+        if (num_groups * n > kMaxDim)
+            return fail(FP8G_ERR_UNSUPPORTED, "num_groups * n must be < 2^31");
+        if (m == 0) {
+            t_last_error.clear();
+            return FP8G_OK;
+        }
+        if ((s = check_ptrs(a, b, a_scale, b_scale, out)) != FP8G_OK) return s;
+        if (!m_indices) return fail(FP8G_ERR_INVALID_ARGUMENT, "m_indices is null");
+        if (!aligned(m_indices, 4))
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "m_indices must be 4-byte aligned");
+        const int64_t tiles = ((m + 127) / 128) * ((n + 255) / 256);
+        if (tiles > kMaxDim) return fail(FP8G_ERR_UNSUPPORTED, "problem has too many tiles");
+        DeviceState* ds = nullptr;
+        if ((s = device_state(&ds)) != FP8G_OK) return s;
+        CUtensorMap map_a, map_b;
+        if ((s = encode_map(&map_a, a, m, k, fp8g::BLOCK_M, "a")) != FP8G_OK) return s;
+        if ((s = encode_map(&map_b, b, num_groups * n, k, fp8g::BLOCK_N, "b")) != FP8G_OK)
+            return s;
+        Params p = base_params(a_scale, b_scale, out, m, n, k);
+        p.num_tiles = static_cast<int>(tiles);
+        p.num_groups = static_cast<int>(num_groups);
+        p.m_indices = m_indices;
+        p.status = ds->status;
+        return launch<fp8g::FORM_GROUPED, __nv_bfloat16>(*ds, 2, map_a, map_b, p, tiles, stream);
+    } catch (...) {
+        return fail(FP8G_ERR_CUDA, "unexpected exception");
+    }
+}
+
+fp8g_status_t fp8_batch_gemm_masked(const void* a, const void* b, const float* a_scale,
+                                    const float* b_scale, const int32_t* masked_m,
+                                    int64_t expected_m, void* out, int64_t num_groups,
+                                    int64_t max_m, int64_t n, int64_t k, cudaStream_t stream) {
+    try {
+        if (num_groups < 0 || max_m < 0)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "num_groups = %lld and max_m = %lld must be >= 0",
+                        (long long)num_groups, (long long)max_m);
+        if (expected_m < 0)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "expected_m = %lld < 0", (long long)expected_m);
+        fp8g_status_t s = check_nk(n, k);
+        if (s != FP8G_OK) return s;
+        if (num_groups * max_m > kMaxDim || num_groups * n > kMaxDim)
+            return fail(FP8G_ERR_UNSUPPORTED, "num_groups * max_m and num_groups * n must be < 2^31");
+        const int64_t tiles = num_groups * ((max_m + 127) / 128) * ((n + 255) / 256);
+        if (tiles > kMaxDim) return fail(FP8G_ERR_UNSUPPORTED, "problem has too many tiles");
+        if (tiles == 0) {
+            t_last_error.clear();
+            return FP8G_OK;
+        }
+        if ((s = check_ptrs(a, b, a_scale, b_scale, out)) != FP8G_OK) return s;
+        if (!masked_m) return fail(FP8G_ERR_INVALID_ARGUMENT, "masked_m is null");
+        if (!aligned(masked_m, 4))
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "masked_m must be 4-byte aligned");
+        DeviceState* ds = nullptr;
+        if ((s = device_state(&ds)) != FP8G_OK) return s;
+        CUtensorMap map_a, map_b;
+        if ((s = encode_map(&map_a, a, num_groups * max_m, k, fp8g::BLOCK_M, "a")) != FP8G_OK)
+            return s;
+        if ((s = encode_map(&map_b, b, num_groups * n, k, fp8g::BLOCK_N, "b")) != FP8G_OK)
+            return s;
+        Params p = base_params(a_scale, b_scale, out, max_m, n, k);
+        p.num_tiles = static_cast<int>(tiles);  // upper bound; the kernel walks masked_m
+        p.num_groups = static_cast<int>(num_groups);
+        p.masked_m = masked_m;
+        p.status = ds->status;
+        return launch<fp8g::FORM_MASKED, __nv_bfloat16>(*ds, 3, map_a, map_b, p, tiles, stream);
+    } catch (...) {
+        return fail(FP8G_ERR_CUDA, "unexpected exception");
+    }
+}
+
+fp8g_status_t fp8g_get_device_status(unsigned int* flags, int clear) {
+    try {
+        if (!flags) return fail(FP8G_ERR_INVALID_ARGUMENT, "flags is null");
+        DeviceState* ds = nullptr;
+        fp8g_status_t s = device_state(&ds);
+        if (s != FP8G_OK) return s;
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+        unsigned int v = 0;
+        e = cudaMemcpy(&v, ds->status, sizeof(v), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+        if (clear) {
+            e = cudaMemset(ds->status, 0, sizeof(unsigned int));
+            if (e == cudaSuccess) e = cudaDeviceSynchronize();
+            if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+        }
+        *flags = v;
+        if (v & FP8G_DEVICE_TIMEOUT)
+            return fail(FP8G_ERR_TIMEOUT, "a kernel gave up waiting on its pipeline (timeout)");
+        t_last_error.clear();
+        return FP8G_OK;
+    } catch (...) {
+        return fail(FP8G_ERR_CUDA, "unexpected exception");
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,496 @@
+// Persistent, warp-specialised FP8 (E4M3) groupwise-scaled NT GEMM for sm_103a.
+//
+// Computes the operation of the MATE page "FlashInfer Wrapper APIs", section
+// GEMM (gemm_fp8_nt_groupwise and its grouped/masked MoE forms):
+//   out[i][j] = sum_kb P(i,j,kb) * a_scale(i,kb) * b_scale(j/128,kb),
+//   P(i,j,kb) = sum over the 128 k of block kb of a[i][k] * b[j][k].
+//
+// One CTA per SM walks output tiles of 128 x 256.  Per tile and per 128-wide
+// K block (one scale block):
+//   warp 0      TMA producer: loads the A (128x128) and B (256x128) E4M3 tiles
+//               into a 4-stage ring of 128-byte-swizzled shared-memory slots.
+//   warp 1      MMA issuer: 4 x tcgen05.mma (K = 32) write the block's partial
+//               sums P into one of two TMEM buffers (FP32, 128 lanes x 256 cols),
+//               fresh for every K block.
+//   warps 2-3   idle (they complete the first warpgroup).
+//   warps 4-11  promotion + epilogue: read the partial from TMEM, multiply by
+//               a_scale(row,kb) * b_scale(col block,kb) and accumulate in FP32
+//               registers (one row per thread, 128 columns per warpgroup);
+//               after the last K block convert to BF16/FP16 and store the row.
+// The 128 x 256 FP32 running sums take half of the register file, so the
+// control warpgroup hands registers to the two promotion warpgroups
+// (setmaxnreg: 56 + 2 x 224 per thread, exactly the launch's 3 x 168).
+// The two TMEM buffers let the tensor cores compute block kb+1 while block kb
+// is being promoted, and the next tile's first blocks while the epilogue runs.
+//
+// Every wait on a pipeline barrier is bounded: past the limit the waiting warp
+// raises an abort flag shared by the CTA and a bit in the device status word,
+// all roles leave their loops, in-flight copies and MMAs are drained, TMEM is
+// freed and the kernel returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <limits.h>
+#include <stdint.h>
+
+#include "fp8g.h"
+#include "ptx.cuh"
+
+namespace fp8g {
+
+constexpr int BLOCK_M = 128;  // tile rows = TMEM lanes = UMMA M
+constexpr int BLOCK_N = 256;  // tile columns = UMMA N
+constexpr int BLOCK_K = 128;  // one scale block along k = one 128-byte swizzle row of E4M3
+constexpr int UMMA_K = 32;    // K of one kind::f8f6f4 instruction
+constexpr int STAGES = 4;
+constexpr int NUM_PROMO_WARPS = 8;
+constexpr int FIRST_PROMO_WARP = 4;
+constexpr int NUM_THREADS = 128 + 32 * NUM_PROMO_WARPS;  // 3 warpgroups
+constexpr uint32_t LAUNCH_REGS = 168;   // per thread at launch (3 warps per SM sub-partition)
+constexpr uint32_t CONTROL_REGS = 56;   // warpgroup 0 after setmaxnreg.dec
+constexpr uint32_t PROMO_REGS = 224;    // warpgroups 1-2 after setmaxnreg.inc
+static_assert(128 * CONTROL_REGS + 256 * PROMO_REGS <= NUM_THREADS * LAUNCH_REGS,
+              "register split exceeds the launch's registers");
+constexpr int A_TILE_BYTES = BLOCK_M * BLOCK_K;
+constexpr int B_TILE_BYTES = BLOCK_N * BLOCK_K;
+constexpr uint32_t TMEM_COLS = 2 * BLOCK_N;  // two FP32 partial buffers
+constexpr int BAR_BYTES = 256;               // barriers, TMEM slot, abort flag
+constexpr size_t SMEM_BYTES = 1024 /* alignment slack */ +
+                              size_t(STAGES) * (A_TILE_BYTES + B_TILE_BYTES) + BAR_BYTES;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s: far beyond any legitimate wait
+constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
+
+enum Form { FORM_DENSE = 0, FORM_GROUPED = 1, FORM_MASKED = 2 };
+
+struct Params {
+    const float* a_scale;
+    const float* b_scale;
+    void* out;
+    const int32_t* m_indices;  // grouped form
+    const int32_t* masked_m;   // masked form
+    unsigned int* status;      // device status word
+    int rows;                  // dense: m; grouped: M_total; masked: max_m
+    int n, k;
+    int kblocks, nblocks;  // k/128, n/128
+    int n_tiles;           // ceil(n / BLOCK_N)
+    int m_blocks;          // ceil(rows / BLOCK_M)
+    int num_tiles;         // dense/grouped: m_blocks * n_tiles
+    int num_groups;
+    int scale_mn_major;  // dense form only
+    int band_m;          // m-blocks per raster band (dense/grouped)
+};
+
+// One output tile as every role sees it.
+struct Tile {
+    int mb, nb;          // 128-row block (within the group for the masked form), 256-col block
+    int group;           // expert (grouped) or group (masked); 0 for dense
+    int a_row0, b_row0;  // first row of the tile in the 2-D views of a and b
+    int group_rows;      // masked: valid rows of the group
+    int row_expert[4];   // grouped: m_indices of rows 32q + lane, q = 0..3
+    bool skip;           // grouped: padding-only block or broken precondition
+};
+
+// Maps tile ids to tiles.  All roles walk the same ids (blockIdx.x, +gridDim.x,
+// ...) through identical schedulers, so they agree on every tile.  Called by
+// whole warps (the grouped form reduces over the warp).
+template <int FORM>
+struct Scheduler {
+    const Params& p;
+    int g = 0;     // masked: group the cursor is in
+    int base = 0;  // masked: first tile id of group g
+    __device__ explicit Scheduler(const Params& params) : p(params) {}
+
+    __device__ int masked_rows(int grp, bool flag) const {
+        const int v = __ldg(p.masked_m + grp);
+        const int c = min(max(v, 0), p.rows);
+        if (flag && c != v) atomicOr(p.status, FP8G_DEVICE_MASKED_M_CLAMPED);
+        return c;
+    }
+
+    // Dense and grouped: raster of bands of `band_m` m-blocks; inside a band the
+    // m-block varies fastest, so the CTAs running at one time share A row panels
+    // and B column panels in L2.
+    __device__ void raster(int t, int& mb, int& nb) const {
+        const int per_band = p.band_m * p.n_tiles;
+        const int band = t / per_band;
+        const int rem = t - band * per_band;
+        const int in_band = min(p.band_m, p.m_blocks - band * p.band_m);
+        nb = rem / in_band;
+        mb = band * p.band_m + rem % in_band;
+    }
+
+    // False once t is past the last tile.  `flag` lets one thread report
+    // precondition violations in the device status word.
+    __device__ bool next(int t, Tile& tile, bool flag) {
+        tile.skip = false;
+        tile.group = 0;
+        tile.group_rows = 0;
+        if constexpr (FORM == FORM_MASKED) {
+            while (g < p.num_groups) {
+                const int rows_g = masked_rows(g, flag && blockIdx.x == 0);
+                const int mbk = (rows_g + BLOCK_M - 1) / BLOCK_M;
+                const int count = mbk * p.n_tiles;
+                if (t < base + count) {
+                    const int local = t - base;
+                    tile.nb = local / mbk;  // m-blocks of one n-block are adjacent ids
+                    tile.mb = local - tile.nb * mbk;
+                    tile.group = g;
+                    tile.group_rows = rows_g;
+                    tile.a_row0 = g * p.rows + tile.mb * BLOCK_M;
+                    tile.b_row0 = g * p.n + tile.nb * BLOCK_N;
+                    return true;
+                }
+                base += count;
+                ++g;
+            }
+            return false;
+        } else {
+            if (t >= p.num_tiles) return false;
+            raster(t, tile.mb, tile.nb);
+            tile.a_row0 = tile.mb * BLOCK_M;
+            tile.b_row0 = tile.nb * BLOCK_N;
+            if constexpr (FORM == FORM_GROUPED) {
+                const int lane = threadIdx.x & 31;
+                int lo = INT_MAX, hi = -1, bad = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int row = tile.a_row0 + q * 32 + lane;
+                    const int e = row < p.rows ? __ldg(p.m_indices + row) : -1;
+                    tile.row_expert[q] = e;
+                    if (e < -1 || e >= p.num_groups) {
+                        bad = 1;
+                    } else if (e >= 0) {
+                        lo = min(lo, e);
+                        hi = max(hi, e);
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+                    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+                    bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+                }
+                const bool mixed = hi >= 0 && lo != hi;
+                if (flag && (bad || mixed)) atomicOr(p.status, FP8G_DEVICE_BAD_M_INDICES);
+                tile.skip = bad || mixed || hi < 0;
+                tile.group = hi;
+                tile.b_row0 = hi * p.n + tile.nb * BLOCK_N;
+            }
+            return true;
+        }
+    }
+};
+
+struct Ctl {
+    volatile int* abort_flag;
+    unsigned int* status;
+};
+
+// Wait for the phase of `bar` with the given parity; false if the CTA aborted
+// or this wait exceeded its limit (which aborts the CTA).
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const Ctl& c) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((spin & 31u) == 0) {
+            if (*c.abort_flag) return false;
+            if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+                *c.abort_flag = 1;
+                atomicOr(c.status, FP8G_DEVICE_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// All lanes wait; the warp gives up together if any lane gave up.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Ctl& c) {
+    const bool ok = wait_phase(bar, parity, c);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait used only while draining at exit (ignores the abort flag).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > DRAIN_LIMIT_NS) break;
+}
+
+template <int FORM>
+__device__ __forceinline__ void run_producer(const CUtensorMap* map_a, const CUtensorMap* map_b,
+                                             const Params& p, uint8_t* sA, uint8_t* sB,
+                                             uint64_t* full, uint64_t* empty, const Ctl& ctl) {
+    const int lane = threadIdx.x & 31;
+    Scheduler<FORM> sched(p);
+    int stage = 0;
+    uint32_t phase = 0, armed = 0, armed_parity = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok; t += gridDim.x) {
+        Tile tile;
+        if (!sched.next(t, tile, lane == 0)) break;
+        if (tile.skip) continue;
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+            if (!warp_wait(empty + stage, phase ^ 1u, ctl)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full + stage, A_TILE_BYTES + B_TILE_BYTES);
+                tma_load_2d(sA + stage * A_TILE_BYTES, map_a, full + stage, kb * BLOCK_K,
+                            tile.a_row0);
+                tma_load_2d(sB + stage * B_TILE_BYTES, map_b, full + stage, kb * BLOCK_K,
+                            tile.b_row0);
+            }
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            __syncwarp();
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // Every copy issued must have landed before shared memory is released.
+    if (lane == 0)
+        for (int s = 0; s < STAGES; ++s)
+            if ((armed >> s) & 1u) drain_wait(full + s, (armed_parity >> s) & 1u);
+    __syncwarp();
+}
+
+template <int FORM>
+__device__ __forceinline__ void run_mma(const Params& p, uint8_t* sA, uint8_t* sB, uint64_t* full,
+                                        uint64_t* empty, uint64_t* acc_full, uint64_t* acc_empty,
+                                        uint64_t* drain, uint32_t tmem_base, const Ctl& ctl) {
+    const int lane = threadIdx.x & 31;
+    constexpr uint32_t IDESC = idesc_e4m3_f32(BLOCK_M, BLOCK_N);
+    Scheduler<FORM> sched(p);
+    int stage = 0, buf = 0;
+    uint32_t phase = 0, bphase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok; t += gridDim.x) {
+        Tile tile;
+        if (!sched.next(t, tile, false)) break;
+        if (tile.skip) continue;
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+            if (!warp_wait(acc_empty + buf, bphase ^ 1u, ctl) ||
+                !warp_wait(full + stage, phase, ctl)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            if (lane == 0) {
+                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BLOCK_N);
+                const uint64_t ad = smem_desc_k_sw128(smem_u32(sA + stage * A_TILE_BYTES));
+                const uint64_t bd = smem_desc_k_sw128(smem_u32(sB + stage * B_TILE_BYTES));
+#pragma unroll
+                for (int kk = 0; kk < BLOCK_K / UMMA_K; ++kk) {
+                    // advance the start address by kk * 32 bytes inside the swizzled rows
+                    const uint64_t step = static_cast<uint64_t>((kk * UMMA_K) >> 4);
+                    umma_f8f6f4(d, ad + step, bd + step, IDESC, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(empty + stage);   // smem slot free once these MMAs finish
+                umma_commit(acc_full + buf);  // partial ready for promotion
+            }
+            __syncwarp();
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            if (++buf == 2) {
+                buf = 0;
+                bphase ^= 1u;
+            }
+        }
+    }
+    // All MMAs issued must have completed before TMEM and shared memory go away.
+    if (lane == 0) {
+        umma_commit(drain);
+        drain_wait(drain, 0);
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16*) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __half*) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 128 consecutive outputs of one row, 16-byte stores.
+template <typename OutT>
+__device__ __forceinline__ void store_row128(OutT* dst, const float (&acc)[128]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        uint4 v;
+        v.x = pack2(acc[8 * i + 0], acc[8 * i + 1], static_cast<OutT*>(nullptr));
+        v.y = pack2(acc[8 * i + 2], acc[8 * i + 3], static_cast<OutT*>(nullptr));
+        v.z = pack2(acc[8 * i + 4], acc[8 * i + 5], static_cast<OutT*>(nullptr));
+        v.w = pack2(acc[8 * i + 6], acc[8 * i + 7], static_cast<OutT*>(nullptr));
+        reinterpret_cast<uint4*>(dst)[i] = v;
+    }
+}
+
+__device__ __forceinline__ float load_scale(const float* sa, int sa_step, const float* sb,
+                                            int sb_step, int kb) {
+    const float x = sa ? __ldg(sa + static_cast<int64_t>(kb) * sa_step) : 0.0f;
+    const float y = sb ? __ldg(sb + static_cast<int64_t>(kb) * sb_step) : 0.0f;
+    return x * y;
+}
+
+template <int FORM, typename OutT>
+__device__ __forceinline__ void run_promotion(const Params& p, uint64_t* acc_full,
+                                              uint64_t* acc_empty, uint32_t tmem_base,
+                                              const Ctl& ctl) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int quarter = warp & 3;       // this warp may read TMEM lanes 32*quarter .. +31
+    const int half = (warp - FIRST_PROMO_WARP) >> 2;  // which 128 columns of the tile
+    const int r = quarter * 32 + lane;  // row of the tile owned by this thread
+    const int KB = p.kblocks;
+    OutT* out = static_cast<OutT*>(p.out);
+    Scheduler<FORM> sched(p);
+    int buf = 0;
+    uint32_t bphase = 0;
+    for (int t = blockIdx.x;; t += gridDim.x) {
+        Tile tile;
+        if (!sched.next(t, tile, false)) break;
+        if (tile.skip) continue;
+
+        const int jb = tile.nb * (BLOCK_N / 128) + half;  // 128-column scale block
+        const bool col_ok = jb < p.nblocks;
+        const int col0 = tile.nb * BLOCK_N + half * 128;
+        int64_t out_row;
+        bool row_ok;
+        const float *sa = nullptr, *sb = nullptr;
+        int sa_step = 1, sb_step = 1;
+        if constexpr (FORM == FORM_MASKED) {
+            const int rin = tile.mb * BLOCK_M + r;
+            out_row = static_cast<int64_t>(tile.group) * p.rows + rin;
+            row_ok = rin < tile.group_rows;
+            if (rin < p.rows) sa = p.a_scale + out_row * KB;
+            if (col_ok) sb = p.b_scale + (static_cast<int64_t>(tile.group) * p.nblocks + jb) * KB;
+        } else {
+            out_row = static_cast<int64_t>(tile.mb) * BLOCK_M + r;
+            const bool row_in = out_row < p.rows;
+            if constexpr (FORM == FORM_GROUPED) {
+                row_ok = row_in && tile.row_expert[quarter] == tile.group;
+                if (row_in) sa = p.a_scale + out_row * KB;
+                if (col_ok)
+                    sb = p.b_scale + (static_cast<int64_t>(tile.group) * p.nblocks + jb) * KB;
+            } else {
+                row_ok = row_in;
+                if (p.scale_mn_major) {
+                    if (row_in) sa = p.a_scale + out_row, sa_step = p.rows;
+                    if (col_ok) sb = p.b_scale + jb, sb_step = p.nblocks;
+                } else {
+                    if (row_in) sa = p.a_scale + out_row * KB;
+                    if (col_ok) sb = p.b_scale + static_cast<int64_t>(jb) * KB;
+                }
+            }
+        }
+
+        float acc[128];
+#pragma unroll
+        for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+        float s_next = load_scale(sa, sa_step, sb, sb_step, 0);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+            const float s = s_next;
+            if (kb + 1 < KB) s_next = load_scale(sa, sa_step, sb, sb_step, kb + 1);
+            if (!warp_wait(acc_full + buf, bphase, ctl)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(buf * BLOCK_N + half * 128);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tmem_load_32cols(taddr + c * 32, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    acc[c * 32 + i] = fmaf(__uint_as_float(v[i]), s, acc[c * 32 + i]);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + buf);
+            if (++buf == 2) {
+                buf = 0;
+                bphase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        if (row_ok && col_ok) store_row128(out + out_row * p.n + col0, acc);
+    }
+}
+
+template <int FORM, typename OutT>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * A_TILE_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_TILE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* acc_full = empty + STAGES;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full + b, 1);
+            mbar_init(acc_empty + b, NUM_PROMO_WARPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        mbar_init_fence();
+    }
+    if (threadIdx.x == 32) {
+        tma_prefetch_map(&map_a);
+        tma_prefetch_map(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+    const Ctl ctl{abort_flag, p.status};
+
+    if (warp < FIRST_PROMO_WARP) {
+        regs_dec<CONTROL_REGS>();
+        if (warp == 0)
+            run_producer<FORM>(&map_a, &map_b, p, sA, sB, full, empty, ctl);
+        else if (warp == 1)
+            run_mma<FORM>(p, sA, sB, full, empty, acc_full, acc_empty, drain, tmem_base, ctl);
+    } else {
+        regs_inc<PROMO_REGS>();
+        run_promotion<FORM, OutT>(p, acc_full, acc_empty, tmem_base, ctl);
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace fp8g

@@ -1,0 +1,157 @@
+/*
+ * fp8g — FP8 (E4M3) groupwise-scaled NT GEMM for sm_103a (GB300).
+ *
+ * C ABI of the library.  Three operations, as defined on the MATE page
+ * "FlashInfer Wrapper APIs", section GEMM:
+ *
+ *   fp8_gemm_nt_groupwise       gemm_fp8_nt_groupwise            out = a @ b.T
+ *   fp8_group_gemm_contiguous   group_deepgemm_fp8_nt_groupwise  out[i] = a[i] @ b[m_indices[i]].T
+ *   fp8_batch_gemm_masked       batch_deepgemm_fp8_nt_groupwise  out[g,:masked_m[g]] = a[g,:masked_m[g]] @ b[g].T
+ *
+ * Scaling is groupwise at granularity (1, 128, 128): with KB = k/128,
+ *   out[i][j] = sum_kb ( sum_{t in block kb} a[i][t] * b[j][t] ) * a_scale(i, kb) * b_scale(j/128, kb)
+ * where a and b hold E4M3 (float8_e4m3fn) codes and the scales are FP32
+ * multipliers (dequantisation factors).  Block sums are accumulated in FP32 on
+ * the tensor cores, scaled and summed in FP32, and rounded once to the output
+ * type (round to nearest even).
+ *
+ * Conventions, shared by every entry point (the ownership and error model of
+ * the "flashmla-rs" page, section Design Notes, and the asynchronous calls of
+ * the "flashinfer-rs" page, section Additional Notes):
+ *   - All array arguments are DEVICE pointers owned by the caller.  The
+ *     library allocates nothing per call and keeps no pointer after return.
+ *   - Work is enqueued on `stream` and the call returns without synchronising.
+ *     Results are ready when the stream reaches that point.
+ *   - Every argument is checked on the host before anything is launched; a
+ *     rejected call launches nothing and leaves `out` untouched.  No C++
+ *     exception crosses the ABI.  On failure the return value says why and
+ *     fp8g_last_error() gives a message.
+ *   - Device requirements: compute capability 10.3 (sm_103, GB300), else
+ *     FP8G_ERR_ARCH.
+ *   - Shapes: k and n must be positive multiples of 128 (the scale
+ *     granularity); m (and max_m, M_total) may be any non-negative value,
+ *     including 0 (nothing is launched).  Every dimension must be < 2^31.
+ *   - Alignment: a, b and out 16-byte aligned; scales 4-byte aligned;
+ *     m_indices / masked_m 4-byte aligned.  All arrays densely packed
+ *     (contiguous, row-major, no padding between rows).
+ *   - Calls are thread-safe.  Calls on different streams may run concurrently.
+ */
+#ifndef FP8G_H
+#define FP8G_H
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8G_OK = 0,
+    FP8G_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad shape, misalignment, bad enum */
+    FP8G_ERR_UNSUPPORTED = 2,      /* valid on the page but not provided here */
+    FP8G_ERR_ARCH = 3,             /* current device is not sm_103 */
+    FP8G_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed */
+    FP8G_ERR_TIMEOUT = 5           /* reported through the device status word */
+} fp8g_status_t;
+
+/* Scale layout of the dense form (page: scale_major_mode; None means "K").
+ *   K-major:  a_scale (m, k/128),   b_scale (n/128, k/128)
+ *   MN-major: a_scale (k/128, m),   b_scale (k/128, n/128)              */
+typedef enum { FP8G_SCALE_K_MAJOR = 0, FP8G_SCALE_MN_MAJOR = 1 } fp8g_scale_major_t;
+
+/* Output element type: BF16 (the page's default) or FP16. */
+typedef enum { FP8G_OUT_BF16 = 0, FP8G_OUT_F16 = 1 } fp8g_dtype_t;
+
+/* Bits of the device status word (see fp8g_get_device_status). */
+#define FP8G_DEVICE_TIMEOUT 0x1u          /* a pipeline wait exceeded its limit; the launch gave up */
+#define FP8G_DEVICE_BAD_M_INDICES 0x2u    /* a 128-row block broke the contiguous-layout precondition; skipped */
+#define FP8G_DEVICE_MASKED_M_CLAMPED 0x4u /* some masked_m[g] was outside [0, max_m]; clamped */
+
+/*
+ * Dense groupwise FP8 NT GEMM (page: gemm_fp8_nt_groupwise).
+ *
+ *   a        (m, k)  E4M3 codes, row-major.
+ *   b        (n, k)  E4M3 codes, row-major; the operation is a @ b.T.
+ *   a_scale  FP32, (m, k/128) if K-major, (k/128, m) if MN-major.
+ *   b_scale  FP32, (n/128, k/128) if K-major, (k/128, n/128) if MN-major.
+ *   out      (m, n) row-major, BF16 or FP16 per out_dtype.  Every element is
+ *            written.
+ *   gran_m, gran_n, gran_k   the page's scale_granularity_mnk; only
+ *            (1, 128, 128) is provided, anything else is FP8G_ERR_UNSUPPORTED.
+ *   mma_sm   the page's MMA configuration hint: 0 (auto), 1 or 2.  It may
+ *            change speed, never results.
+ */
+fp8g_status_t fp8_gemm_nt_groupwise(const void* a, const void* b,
+                                    const float* a_scale, const float* b_scale,
+                                    void* out, fp8g_dtype_t out_dtype,
+                                    int64_t m, int64_t n, int64_t k,
+                                    fp8g_scale_major_t scale_major,
+                                    int gran_m, int gran_n, int gran_k,
+                                    int mma_sm, cudaStream_t stream);
+
+/*
+ * Contiguous grouped FP8 NT GEMM for MoE experts
+ * (page: group_deepgemm_fp8_nt_groupwise).
+ *
+ *   a          (m, k) E4M3, the rows of all experts stacked (m = M_total).
+ *   b          (num_groups, n, k) E4M3 expert weights.
+ *   a_scale    FP32 (m, k/128), K-major.
+ *   b_scale    FP32 (num_groups, n/128, k/128), K-major.
+ *   m_indices  int32 (m): the expert of each row, -1 for a padding row.
+ *              Precondition (page): each expert's rows occupy a contiguous
+ *              region starting on a multiple of 128 rows, so every 128-row
+ *              block holds rows of at most one expert plus -1 padding.
+ *   out        (m, n) BF16.  Rows with m_indices == -1 are not written (the
+ *              page leaves them unspecified).
+ *   A block that breaks the precondition (an id outside [-1, num_groups) or
+ *   two experts in one block) is skipped, not written, and raises
+ *   FP8G_DEVICE_BAD_M_INDICES in the device status word; it never faults.
+ */
+fp8g_status_t fp8_group_gemm_contiguous(const void* a, const void* b,
+                                        const float* a_scale, const float* b_scale,
+                                        const int32_t* m_indices, void* out,
+                                        int64_t m, int64_t n, int64_t k,
+                                        int64_t num_groups, cudaStream_t stream);
+
+/*
+ * Masked batched FP8 NT GEMM for MoE decode
+ * (page: batch_deepgemm_fp8_nt_groupwise).
+ *
+ *   a          (num_groups, max_m, k) E4M3.
+ *   b          (num_groups, n, k) E4M3.
+ *   a_scale    FP32 (num_groups, max_m, k/128), K-major.
+ *   b_scale    FP32 (num_groups, n/128, k/128), K-major.
+ *   masked_m   int32 (num_groups), device memory: valid rows per group.
+ *              Values outside [0, max_m] are clamped and raise
+ *              FP8G_DEVICE_MASKED_M_CLAMPED.
+ *   expected_m the page's host-side row-count hint (>= 0).  It may change
+ *              speed, never results.
+ *   out        (num_groups, max_m, n) BF16.  Rows at or beyond masked_m[g] are
+ *              not written (the page leaves them unspecified).
+ */
+fp8g_status_t fp8_batch_gemm_masked(const void* a, const void* b,
+                                    const float* a_scale, const float* b_scale,
+                                    const int32_t* masked_m, int64_t expected_m,
+                                    void* out, int64_t num_groups, int64_t max_m,
+                                    int64_t n, int64_t k, cudaStream_t stream);
+
+/* Message of the last failed call on this thread ("" if none); valid until the
+ * thread's next call into the library. */
+const char* fp8g_last_error(void);
+
+/*
+ * Device status word of the current device: an OR of FP8G_DEVICE_* bits set by
+ * kernels since it was last cleared.  Synchronises the device first, then
+ * copies the word to *flags and, if `clear` is non-zero, resets it.  Returns
+ * FP8G_ERR_TIMEOUT if the timeout bit is set, FP8G_OK otherwise (other bits
+ * are reported through *flags only).
+ */
+fp8g_status_t fp8g_get_device_status(unsigned int* flags, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8G_H */

@@ -1,0 +1,131 @@
+"""The C-ABI library on a host without a GPU: it loads, exports every entry
+point that include/fp8g.h declares, and rejects bad arguments on the host with
+the documented status codes, before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8g.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_block_scaled_nt_gb300 import _build
+    _build.build()
+    import fp8_block_scaled_nt_gb300 as fp8g
+    return fp8g
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_three_forms_and_helpers():
+    names = declared_functions()
+    for f in ("fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
+              "fp8g_last_error", "fp8g_get_device_status"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    handle = lib.load()
+    for name in declared_functions():
+        assert hasattr(handle, name), name
+
+
+def test_header_compiles_as_c():
+    import subprocess
+    import tempfile
+    from fp8_block_scaled_nt_gb300 import _build
+    inc = os.path.join(_build.cuda_home(), "include")
+    src = '#include "fp8g.h"\nint main(void){ return (int)FP8G_OK; }\n'
+    with tempfile.TemporaryDirectory() as d:
+        p = os.path.join(d, "t.c")
+        open(p, "w").write(src)
+        r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                            "-I", inc, "-c", p, "-o", os.path.join(d, "t.o")],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
+def _dense(h, a=16, b=16, sa=16, sb=16, out=16, dt=0, m=128, n=256, k=256, major=0,
+           gran=(1, 128, 128), mma_sm=1):
+    return h.fp8_gemm_nt_groupwise(a, b, sa, sb, out, dt, m, n, k, major, gran[0], gran[1],
+                                   gran[2], mma_sm, None)
+
+
+@pytest.mark.parametrize("kwargs,status,msg", [
+    (dict(k=200), 1, "k = 200"),
+    (dict(k=0), 1, "k = 0"),
+    (dict(n=192), 1, "n = 192"),
+    (dict(m=-1), 1, "m = -1"),
+    (dict(dt=7), 1, "out_dtype"),
+    (dict(major=3), 1, "scale_major"),
+    (dict(mma_sm=5), 1, "mma_sm"),
+    (dict(gran=(1, 128, 64)), 2, "granularity"),
+    (dict(a=0), 1, "null"),
+    (dict(out=0), 1, "null"),
+    (dict(b=24), 1, "16-byte"),
+    (dict(sa=18), 1, "4-byte"),
+    (dict(n=1 << 31), 2, "2^31"),
+])
+def test_dense_host_validation(lib, kwargs, status, msg):
+    h = lib.load()
+    assert _dense(h, **kwargs) == status
+    assert msg in lib.last_error()
+
+
+def test_empty_problem_is_ok_without_device(lib):
+    h = lib.load()
+    assert _dense(h, m=0, a=0, out=0, sa=0) == 0
+    assert h.fp8_batch_gemm_masked(16, 16, 16, 16, 16, 1, 16, 0, 256, 256, 256, None) == 0
+    assert h.fp8_group_gemm_contiguous(0, 16, 0, 16, 0, 0, 0, 256, 256, 4, None) == 0
+
+
+def test_grouped_host_validation(lib):
+    h = lib.load()
+    assert h.fp8_group_gemm_contiguous(16, 16, 16, 16, 16, 16, 256, 256, 256, 0, None) == 1
+    assert "num_groups" in lib.last_error()
+    assert h.fp8_group_gemm_contiguous(16, 16, 16, 16, 0, 16, 256, 256, 256, 4, None) == 1
+    assert "m_indices" in lib.last_error()
+    assert h.fp8_group_gemm_contiguous(16, 16, 16, 16, 18, 16, 256, 256, 256, 4, None) == 1
+    assert h.fp8_group_gemm_contiguous(16, 16, 16, 16, 16, 16, 256, 256, 100, 4, None) == 1
+
+
+def test_masked_host_validation(lib):
+    h = lib.load()
+    assert h.fp8_batch_gemm_masked(16, 16, 16, 16, 16, -1, 16, 4, 256, 256, 256, None) == 1
+    assert "expected_m" in lib.last_error()
+    assert h.fp8_batch_gemm_masked(16, 16, 16, 16, 0, 1, 16, 4, 256, 256, 256, None) == 1
+    assert "masked_m" in lib.last_error()
+    assert h.fp8_batch_gemm_masked(16, 16, 16, 16, 16, 1, 16, -1, 256, 256, 256, None) == 1
+
+
+def test_valid_call_without_a_device_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host has a GPU")
+    h = lib.load()
+    assert _dense(h) == 4  # FP8G_ERR_CUDA: no device, nothing launched
+    assert "cudaGetDevice" in lib.last_error()
+    flags = ctypes.c_uint(0)
+    assert h.fp8g_get_device_status(ctypes.byref(flags), 0) == 4
+
+
+def test_binding_rejects_bad_tensors_before_the_library(lib):
+    import torch
+    a = torch.zeros((128, 256), dtype=torch.float32)
+    with pytest.raises(TypeError):
+        lib.fp8_gemm_nt_groupwise(a, a, a, a, a)
+    a8 = torch.zeros((128, 256), dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        lib.fp8_gemm_nt_groupwise(a8, torch.zeros((256, 128), dtype=torch.uint8),
+                                  torch.ones((128, 2)), torch.ones((2, 2)),
+                                  torch.empty((128, 256), dtype=torch.bfloat16))
+    with pytest.raises(lib.Fp8gError):
+        lib.gemm_fp8_nt_groupwise(a8, a8, None, None, backend="mudnn")

@@ -1,0 +1,182 @@
+"""GPU parity of the dense form (gemm_fp8_nt_groupwise) against the CPU oracle.
+
+Calls go through the C ABI (libfp8g.so via the thin binding); the oracle is fed
+the very same seeded tensors.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from parity import (as_f64, assert_close, bits16, sentinel_like, to_device, written_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(fp8g, w, out_dtype=torch.bfloat16, mma_sm=1, stream=None):
+    d = to_device(w)
+    out = sentinel_like((w["m"], w["n"]), out_dtype, "cuda")
+    fp8g.fp8_gemm_nt_groupwise(d["a"], d["b"], d["a_scale"], d["b_scale"], out,
+                               scale_major=w["scale_major"], mma_sm=mma_sm, stream=stream)
+    torch.cuda.synchronize()
+    return out
+
+
+def _oracle_full(oracle_mod, w, out_dtype):
+    sm = oracle_mod.SCALE_MN_MAJOR if w["scale_major"] == "MN" else oracle_mod.SCALE_K_MAJOR
+    od = oracle_mod.OUT_F16 if out_dtype == torch.float16 else oracle_mod.OUT_BF16
+    return oracle_mod.gemm_nt_groupwise(w["a"], w["b"], w["a_scale"], w["b_scale"], sm, od)
+
+
+def test_small_workload_full_parity(fp8g, oracle_mod):
+    w = workloads.make("dense_128x256x256")
+    out = _run(fp8g, w)
+    ref, bits = _oracle_full(oracle_mod, w, torch.bfloat16)
+    assert written_rows(out).all()
+    assert_close(as_f64(out), ref, "dense 128x256x256")
+    # most elements round to the same BF16 as the exact result
+    assert np.mean(bits16(out) == bits) > 0.5
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("major", ["K", "MN"])
+@pytest.mark.parametrize("mnk", [(200, 384, 384), (1, 128, 128), (7, 256, 640), (129, 640, 256),
+                                 (384, 512, 1152)])
+def test_ragged_shapes_full_parity(fp8g, oracle_mod, mnk, major, out_dtype):
+    m, n, k = mnk
+    w = workloads.dense(m, n, k, seed=m * 7 + n + k, scale_major=major)
+    out = _run(fp8g, w, out_dtype)
+    ref, _ = _oracle_full(oracle_mod, w, out_dtype)
+    assert written_rows(out).all()
+    assert_close(as_f64(out), ref, "dense %s %s" % (mnk, major))
+
+
+def test_multi_wave_full_parity(fp8g, oracle_mod):
+    # more tiles than SMs, several K blocks, m and n tails
+    w = workloads.dense(2100, 2432, 512, seed=77)
+    out = _run(fp8g, w)
+    ref, _ = _oracle_full(oracle_mod, w, torch.bfloat16)
+    assert_close(as_f64(out), ref, "dense 2100x2432x512")
+
+
+@pytest.mark.parametrize("major", ["K", "MN"])
+def test_dense_4096x7168x2048_sampled(fp8g, oracle_mod, major):
+    w = workloads.make("dense_4096x7168x2048", scale_major=major)
+    out = _run(fp8g, w)
+    assert written_rows(out).all()
+    r, c = workloads.sample_positions(w["m"], w["n"], 65536, seed=11, extra_rows=(0, w["m"] - 1))
+    sm = oracle_mod.SCALE_MN_MAJOR if major == "MN" else oracle_mod.SCALE_K_MAJOR
+    ref, _ = oracle_mod.gemm_nt_groupwise_at(w["a"], w["b"], w["a_scale"], w["b_scale"], r, c, sm)
+    got = as_f64(out)[r.numpy(), c.numpy()]
+    assert_close(got, ref, "dense 4096x7168x2048 %s" % major)
+
+
+def test_dense_16384x18432x7168_f16_sampled(fp8g, oracle_mod):
+    w = workloads.make("dense_16384x18432x7168", device="cuda")
+    out = torch.empty((w["m"], w["n"]), dtype=torch.float16, device="cuda")
+    fp8g.fp8_gemm_nt_groupwise(w["a"], w["b"], w["a_scale"], w["b_scale"], out)
+    torch.cuda.synchronize()
+    r, c = workloads.sample_positions(w["m"], w["n"], 65536, seed=12, extra_rows=(0, w["m"] - 1))
+    host = {k: w[k].cpu() for k in ("a", "b", "a_scale", "b_scale")}
+    ref, _ = oracle_mod.gemm_nt_groupwise_at(host["a"], host["b"], host["a_scale"],
+                                             host["b_scale"], r, c, out_dtype=oracle_mod.OUT_F16)
+    got = out[r.cuda(), c.cuda()].double().cpu().numpy()
+    assert_close(got, ref, "dense 16384x18432x7168 f16")
+
+
+def test_all_ones_closed_form_exact(fp8g):
+    # a = b = 1.0, power-of-two scales: every partial is exactly 128 and every
+    # product exact, so out = sum_kb 128 * sa * sb exactly.
+    m, n, k = 256, 512, 512
+    a = torch.full((m, k), 0x38, dtype=torch.uint8)
+    b = torch.full((n, k), 0x38, dtype=torch.uint8)
+    g = torch.Generator().manual_seed(5)
+    ea = torch.randint(-4, 3, (m, k // 128), generator=g).float()
+    eb = torch.randint(-4, 3, (n // 128, k // 128), generator=g).float()
+    w = dict(a=a, b=b, a_scale=torch.exp2(ea), b_scale=torch.exp2(eb), m=m, n=n, k=k,
+             scale_major="K")
+    out = _run(fp8g, w)
+    want = (128.0 * torch.exp2(ea)[:, None, :] * torch.exp2(eb).repeat_interleave(128, 0)[None]).sum(-1)
+    assert torch.equal(out.float().cpu(), want.to(torch.bfloat16).float())
+
+
+def test_power_of_two_scaling_doubles_exactly(fp8g):
+    w = workloads.dense(300, 512, 768, seed=90)
+    base = _run(fp8g, w)
+    w2 = dict(w)
+    w2["a_scale"] = w["a_scale"].clone()
+    w2["a_scale"][17] *= 2.0
+    w2["b_scale"] = w["b_scale"].clone()
+    w2["b_scale"][2] *= 0.5
+    out = _run(fp8g, w2)
+    b0, b1 = base.float().cpu(), out.float().cpu()
+    expect = b0.clone()
+    expect[17] *= 2.0
+    expect[:, 256:384] *= 0.5
+    assert torch.equal(b1, expect)
+
+
+def test_layout_equivalence_bit_exact(fp8g):
+    wk = workloads.dense(520, 768, 1024, seed=91, scale_major="K")
+    wm = workloads.dense(520, 768, 1024, seed=91, scale_major="MN")
+    assert np.array_equal(bits16(_run(fp8g, wk)), bits16(_run(fp8g, wm)))
+
+
+@pytest.mark.parametrize("mma_sm", [0, 2])
+def test_mma_sm_hint_does_not_change_results(fp8g, mma_sm):
+    w = workloads.dense(333, 640, 512, seed=92)
+    assert np.array_equal(bits16(_run(fp8g, w, mma_sm=1)), bits16(_run(fp8g, w, mma_sm=mma_sm)))
+
+
+def test_deterministic_and_side_stream(fp8g):
+    w = workloads.dense(640, 1024, 768, seed=93)
+    first = bits16(_run(fp8g, w))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        second = _run(fp8g, w, stream=s)
+    s.synchronize()
+    assert np.array_equal(first, bits16(second))
+
+
+def test_empty_m(fp8g):
+    a = torch.empty((0, 256), dtype=torch.uint8, device="cuda")
+    b = torch.zeros((128, 256), dtype=torch.uint8, device="cuda")
+    out = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+    fp8g.fp8_gemm_nt_groupwise(a, b, torch.empty((0, 2), device="cuda"),
+                               torch.ones((1, 2), device="cuda"), out)
+    torch.cuda.synchronize()
+
+
+def test_page_signature_allocates_out(fp8g, oracle_mod):
+    w = workloads.dense(256, 256, 256, seed=94)
+    d = to_device(w)
+    a8 = d["a"].view(torch.float8_e4m3fn)
+    b8 = d["b"].view(torch.float8_e4m3fn)
+    out = fp8g.gemm_fp8_nt_groupwise(a8, b8, d["a_scale"], d["b_scale"], out_dtype=torch.float16)
+    assert out.dtype == torch.float16 and out.shape == (256, 256)
+    ref, _ = oracle_mod.gemm_nt_groupwise(w["a"], w["b"], w["a_scale"], w["b_scale"],
+                                          out_dtype=oracle_mod.OUT_F16)
+    assert_close(as_f64(out), ref, "page signature")
+
+
+def test_invalid_arguments_launch_nothing(fp8g):
+    w = to_device(workloads.dense(128, 256, 256, seed=95))
+    out = sentinel_like((128, 256), torch.bfloat16, "cuda")
+    with pytest.raises(fp8g.Fp8gError) as e:
+        fp8g.fp8_gemm_nt_groupwise(w["a"], w["b"], w["a_scale"], w["b_scale"], out,
+                                   scale_granularity_mnk=(1, 128, 64))
+    assert e.value.status == fp8g.ERR_UNSUPPORTED
+    lib = fp8g.load()
+    # k not a multiple of 128, straight through the C ABI
+    rc = lib.fp8_gemm_nt_groupwise(w["a"].data_ptr(), w["b"].data_ptr(), w["a_scale"].data_ptr(),
+                                   w["b_scale"].data_ptr(), out.data_ptr(), 0, 128, 256, 200, 0,
+                                   1, 128, 128, 1, None)
+    assert rc == fp8g.ERR_INVALID_ARGUMENT and "k = 200" in fp8g.last_error()
+    # misaligned a
+    rc = lib.fp8_gemm_nt_groupwise(w["a"].data_ptr() + 8, w["b"].data_ptr(),
+                                   w["a_scale"].data_ptr(), w["b_scale"].data_ptr(),
+                                   out.data_ptr(), 0, 128, 256, 256, 0, 1, 128, 128, 1, None)
+    assert rc == fp8g.ERR_INVALID_ARGUMENT
+    torch.cuda.synchronize()
+    assert not written_rows(out).any()
+    assert fp8g.get_device_status() == 0
