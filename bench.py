@@ -289,9 +289,15 @@ def oracle_sample_rate(name, w, seconds, seed=21):
                                                  host["b_scale"], host["masked_m"], gs, rs, cs)
         return time.perf_counter() - t0, (gs, rs, cs), ref, wr
 
-    probe = 1024
-    dt, _, _, _ = run(probe)
-    count = int(max(probe, min(50_000_000, probe * seconds / max(dt, 1e-6))))
+    # grow a probe until it takes a measurable time, then size the sample to
+    # about `seconds` of oracle work
+    count = 4096
+    while True:
+        dt, _, _, _ = run(count)
+        if dt >= min(0.5, seconds / 4) or count >= 50_000_000:
+            break
+        count *= 4
+    count = int(max(count, min(50_000_000, count * seconds / max(dt, 1e-6))))
     dt, pos, ref, wr = run(count)
     flops = 2.0 * host["k"] * int(wr.sum())
     return flops / dt, count, dt, oracle.num_threads(), pos, ref, wr

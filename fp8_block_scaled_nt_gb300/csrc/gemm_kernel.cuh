@@ -19,7 +19,7 @@
 //               after the last K block convert to BF16/FP16 and store the row.
 // The 128 x 256 FP32 running sums take half of the register file, so the
 // control warpgroup hands registers to the two promotion warpgroups
-// (setmaxnreg: 56 + 2 x 224 per thread, exactly the launch's 3 x 168).
+// (setmaxnreg: 40 + 2 x 232 per thread, exactly the launch's 3 x 168).
 // The two TMEM buffers let the tensor cores compute block kb+1 while block kb
 // is being promoted, and the next tile's first blocks while the epilogue runs.
 //
@@ -48,8 +48,8 @@ constexpr int NUM_PROMO_WARPS = 8;
 constexpr int FIRST_PROMO_WARP = 4;
 constexpr int NUM_THREADS = 128 + 32 * NUM_PROMO_WARPS;  // 3 warpgroups
 constexpr uint32_t LAUNCH_REGS = 168;   // per thread at launch (3 warps per SM sub-partition)
-constexpr uint32_t CONTROL_REGS = 56;   // warpgroup 0 after setmaxnreg.dec
-constexpr uint32_t PROMO_REGS = 224;    // warpgroups 1-2 after setmaxnreg.inc
+constexpr uint32_t CONTROL_REGS = 40;   // warpgroup 0 after setmaxnreg.dec
+constexpr uint32_t PROMO_REGS = 232;    // warpgroups 1-2 after setmaxnreg.inc
 static_assert(128 * CONTROL_REGS + 256 * PROMO_REGS <= NUM_THREADS * LAUNCH_REGS,
               "register split exceeds the launch's registers");
 constexpr int A_TILE_BYTES = BLOCK_M * BLOCK_K;
@@ -321,16 +321,18 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, __half*) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// 128 consecutive outputs of one row, 16-byte stores.
+// 128 consecutive outputs of one row (acc2[i] holds columns 2i, 2i+1),
+// 16-byte stores.
 template <typename OutT>
-__device__ __forceinline__ void store_row128(OutT* dst, const float (&acc)[128]) {
+__device__ __forceinline__ void store_row128(OutT* dst, const uint64_t (&acc2)[64]) {
+    OutT* tag = nullptr;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         uint4 v;
-        v.x = pack2(acc[8 * i + 0], acc[8 * i + 1], static_cast<OutT*>(nullptr));
-        v.y = pack2(acc[8 * i + 2], acc[8 * i + 3], static_cast<OutT*>(nullptr));
-        v.z = pack2(acc[8 * i + 4], acc[8 * i + 5], static_cast<OutT*>(nullptr));
-        v.w = pack2(acc[8 * i + 6], acc[8 * i + 7], static_cast<OutT*>(nullptr));
+        v.x = pack2(lo_f32(acc2[4 * i + 0]), hi_f32(acc2[4 * i + 0]), tag);
+        v.y = pack2(lo_f32(acc2[4 * i + 1]), hi_f32(acc2[4 * i + 1]), tag);
+        v.z = pack2(lo_f32(acc2[4 * i + 2]), hi_f32(acc2[4 * i + 2]), tag);
+        v.w = pack2(lo_f32(acc2[4 * i + 3]), hi_f32(acc2[4 * i + 3]), tag);
         reinterpret_cast<uint4*>(dst)[i] = v;
     }
 }
@@ -393,9 +395,9 @@ __device__ __forceinline__ void run_promotion(const Params& p, uint64_t* acc_ful
             }
         }
 
-        float acc[128];
+        uint64_t acc[64];  // FP32 running sums, two columns per register pair
 #pragma unroll
-        for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+        for (int i = 0; i < 64; ++i) acc[i] = 0;
         float s_next = load_scale(sa, sa_step, sb, sb_step, 0);
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
@@ -408,13 +410,14 @@ __device__ __forceinline__ void run_promotion(const Params& p, uint64_t* acc_ful
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(buf * BLOCK_N + half * 128);
+            const uint64_t s2 = splat2(s);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32];
-                tmem_load_32cols(taddr + c * 32, v);
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[64];
+                tmem_load_64cols(taddr + c * 64, v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    acc[c * 32 + i] = fmaf(__uint_as_float(v[i]), s, acc[c * 32 + i]);
+                    acc[c * 32 + i] = ffma2(v[2 * i], v[2 * i + 1], s2, acc[c * 32 + i]);
             }
             tc_fence_before_sync();
             __syncwarp();
