@@ -153,6 +153,22 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(busy)}
 
 
+def max_over_ranks(x, device=None):
+    """Largest value of x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput_tflops(world, flops_per_step, steps, slowest_ms):
+    """Whole-job TFLOP/s: the work of every rank over the slowest rank's time."""
+    return world * flops_per_step * steps / (slowest_ms * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------- workloads
 
 def workload_stats(name, w):
@@ -313,7 +329,7 @@ def run_reference(args):
     import workloads
     w = workloads.make(args.workload, device="cpu")
     total = args.steps + args.warmup
-    per_step = max(0.05, min(5.0, 150.0 / max(total, 1)))
+    per_step = max(0.05, min(5.0, args.cpu_seconds / 2, 150.0 / max(total, 1)))
     # one calibration run sizes the sample so that a step takes about per_step
     rate, count, dt, threads, _, _, _ = oracle_sample_rate(args.workload, w, per_step)
     times = []
@@ -404,10 +420,7 @@ def run_ours(args):
     if status:
         raise RuntimeError("device status %#x after the timed region" % status)
 
-    if world > 1:
-        t = torch.tensor([region_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        region_ms = float(t.item())
+    region_ms = max_over_ranks(region_ms, dev)
 
     # End to end through the C ABI with host buffers: per step, copy the inputs
     # of every call from pinned host memory, run the calls, copy outputs back.
@@ -445,13 +458,8 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
-    e2e_value = flops_step * e2e_steps / (e2e_ms * 1e-3) / 1e12
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_value = world * flops_step * e2e_steps / (float(t.item()) * 1e-3) / 1e12
-
-    value = world * flops_step * args.steps / (region_ms * 1e-3) / 1e12
+    e2e_value = throughput_tflops(world, flops_step, e2e_steps, max_over_ranks(e2e_ms, dev))
+    value = throughput_tflops(world, flops_step, args.steps, region_ms)
     launches = args.steps * calls_per_step
     avg_launch_s = region_ms * 1e-3 / launches
     peaks, peaks_src = load_peaks()
