@@ -252,7 +252,7 @@ def call_args(lib, name, w, stream_handle):
         sm = 1 if w["scale_major"] == "MN" else 0
         return (lib.fp8_gemm_nt_groupwise,
                 (p(w["a"]), p(w["b"]), p(w["a_scale"]), p(w["b_scale"]), p(w["out"]), od,
-                 w["m"], w["n"], w["k"], sm, 1, 128, 128, 1, stream_handle))
+                 w["m"], w["n"], w["k"], sm, 1, 128, 128, 0, stream_handle))
     if kind == "grouped":
         return (lib.fp8_group_gemm_contiguous,
                 (p(w["a"]), p(w["b"]), p(w["a_scale"]), p(w["b_scale"]), p(w["m_indices"]),

@@ -42,7 +42,8 @@ fp8g_status_t cuda_fail(cudaError_t e, const char* what) {
 }
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumKernels = 4;  // dense bf16, dense f16, grouped, masked
+// dense bf16, dense f16 (single CTA), grouped, masked, dense bf16, dense f16 (CTA pair)
+constexpr int kNumKernels = 6;
 
 struct DeviceState {
     bool probed = false;
@@ -50,7 +51,8 @@ struct DeviceState {
     int cc_major = 0, cc_minor = 0;
     int sm_count = 0;
     unsigned int* status = nullptr;
-    bool smem_attr_set[kNumKernels] = {};
+    bool kernel_ready[kNumKernels] = {};
+    int resident[kNumKernels] = {};  // CTAs (or CTA pairs) of a persistent grid
 };
 
 std::mutex g_mutex;
@@ -146,13 +148,27 @@ fp8g_status_t check_ptrs(const void* a, const void* b, const float* a_scale, con
     return FP8G_OK;
 }
 
-template <int FORM, typename OutT>
+template <int FORM, typename OutT, bool PAIR>
 fp8g_status_t launch(DeviceState& ds, int slot, const CUtensorMap& map_a, const CUtensorMap& map_b,
                      const Params& p, int64_t max_tiles, cudaStream_t stream) {
-    auto kernel = fp8g::gemm_kernel<FORM, OutT>;
+    using C = fp8g::Cfg<PAIR>;
+    auto kernel = fp8g::gemm_kernel<FORM, OutT, PAIR>;
+    cudaLaunchAttribute cluster_attr;
+    cluster_attr.id = cudaLaunchAttributeClusterDimension;
+    cluster_attr.val.clusterDim.x = 2;
+    cluster_attr.val.clusterDim.y = 1;
+    cluster_attr.val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(fp8g::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    if (PAIR) {
+        cfg.attrs = &cluster_attr;
+        cfg.numAttrs = 1;
+    }
     {
         std::lock_guard<std::mutex> lock(g_mutex);
-        if (!ds.smem_attr_set[slot]) {
+        if (!ds.kernel_ready[slot]) {
             // The kernel moves registers between its warpgroups (setmaxnreg); that
             // is only safe if it is launched with exactly the budget it was built
             // for, so check the compiled register count before the first launch.
@@ -164,22 +180,35 @@ fp8g_status_t launch(DeviceState& ds, int slot, const CUtensorMap& map_a, const 
                             "kernel built with %d registers per thread, expected %u", attr.numRegs,
                             fp8g::LAUNCH_REGS);
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(fp8g::SMEM_BYTES));
+                                     static_cast<int>(C::SMEM_BYTES));
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-            ds.smem_attr_set[slot] = true;
+            int resident = ds.sm_count;
+            if (PAIR) {
+                // persistent grid: as many CTA pairs as can be resident at once
+                cfg.gridDim = dim3(2, 1, 1);
+                int clusters = 0;
+                e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+                if (clusters < 1)
+                    return fail(FP8G_ERR_UNSUPPORTED, "no CTA pair of this kernel fits an SM pair");
+                resident = clusters;
+            }
+            ds.resident[slot] = resident;
+            ds.kernel_ready[slot] = true;
         }
     }
-    const int grid = static_cast<int>(max_tiles < ds.sm_count ? max_tiles : ds.sm_count);
+    const int64_t units = max_tiles < ds.resident[slot] ? max_tiles : ds.resident[slot];
+    cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? 2 * units : units), 1, 1);
     (void)cudaGetLastError();
-    kernel<<<grid, fp8g::NUM_THREADS, fp8g::SMEM_BYTES, stream>>>(map_a, map_b, p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     t_last_error.clear();
     return FP8G_OK;
 }
 
 Params base_params(const float* a_scale, const float* b_scale, void* out, int64_t rows, int64_t n,
-                   int64_t k) {
+                   int64_t k, int tile_m = fp8g::BLOCK_M) {
     Params p{};
     p.a_scale = a_scale;
     p.b_scale = b_scale;
@@ -190,7 +219,7 @@ Params base_params(const float* a_scale, const float* b_scale, void* out, int64_
     p.kblocks = static_cast<int>(k / 128);
     p.nblocks = static_cast<int>(n / 128);
     p.n_tiles = static_cast<int>((n + fp8g::BLOCK_N - 1) / fp8g::BLOCK_N);
-    p.m_blocks = static_cast<int>((rows + fp8g::BLOCK_M - 1) / fp8g::BLOCK_M);
+    p.m_blocks = static_cast<int>((rows + tile_m - 1) / tile_m);
     p.band_m = 8;
     return p;
 }
@@ -228,21 +257,36 @@ fp8g_status_t fp8_gemm_nt_groupwise(const void* a, const void* b, const float* a
             return FP8G_OK;
         }
         if ((s = check_ptrs(a, b, a_scale, b_scale, out)) != FP8G_OK) return s;
-        const int64_t tiles = ((m + 127) / 128) * ((n + 255) / 256);
-        if (tiles > kMaxDim) return fail(FP8G_ERR_UNSUPPORTED, "problem has too many tiles");
+        const int64_t n_tiles = (n + 255) / 256;
+        if (((m + 127) / 128) * n_tiles > kMaxDim)
+            return fail(FP8G_ERR_UNSUPPORTED, "problem has too many tiles");
         DeviceState* ds = nullptr;
         if ((s = device_state(&ds)) != FP8G_OK) return s;
+        // mma_sm: 1 = one SM per 128x256 tile, 2 = a CTA pair per 256x256 tile
+        // (tcgen05 cta_group::2), 0 = pairs when there are enough 256-row tiles
+        // to give every SM pair work.  Results are identical either way.
+        const int64_t pair_tiles = ((m + 255) / 256) * n_tiles;
+        const bool pair = mma_sm == 2 || (mma_sm == 0 && m > 128 && 2 * pair_tiles >= ds->sm_count);
+        const int tile_m = pair ? 2 * fp8g::BLOCK_M : fp8g::BLOCK_M;
+        const int64_t tiles = ((m + tile_m - 1) / tile_m) * n_tiles;
         CUtensorMap map_a, map_b;
         if ((s = encode_map(&map_a, a, m, k, fp8g::BLOCK_M, "a")) != FP8G_OK) return s;
-        if ((s = encode_map(&map_b, b, n, k, fp8g::BLOCK_N, "b")) != FP8G_OK) return s;
-        Params p = base_params(a_scale, b_scale, out, m, n, k);
+        if ((s = encode_map(&map_b, b, n, k, pair ? fp8g::BLOCK_N / 2 : fp8g::BLOCK_N, "b")) !=
+            FP8G_OK)
+            return s;
+        Params p = base_params(a_scale, b_scale, out, m, n, k, tile_m);
         p.num_tiles = static_cast<int>(tiles);
         p.num_groups = 1;
         p.scale_mn_major = scale_major == FP8G_SCALE_MN_MAJOR;
         p.status = ds->status;
         if (out_dtype == FP8G_OUT_BF16)
-            return launch<fp8g::FORM_DENSE, __nv_bfloat16>(*ds, 0, map_a, map_b, p, tiles, stream);
-        return launch<fp8g::FORM_DENSE, __half>(*ds, 1, map_a, map_b, p, tiles, stream);
+            return pair ? launch<fp8g::FORM_DENSE, __nv_bfloat16, true>(*ds, 4, map_a, map_b, p,
+                                                                        tiles, stream)
+                        : launch<fp8g::FORM_DENSE, __nv_bfloat16, false>(*ds, 0, map_a, map_b, p,
+                                                                         tiles, stream);
+        return pair ? launch<fp8g::FORM_DENSE, __half, true>(*ds, 5, map_a, map_b, p, tiles, stream)
+                    : launch<fp8g::FORM_DENSE, __half, false>(*ds, 1, map_a, map_b, p, tiles,
+                                                              stream);
     } catch (...) {
         return fail(FP8G_ERR_CUDA, "unexpected exception");
     }
@@ -283,7 +327,7 @@ fp8g_status_t fp8_group_gemm_contiguous(const void* a, const void* b, const floa
         p.num_groups = static_cast<int>(num_groups);
         p.m_indices = m_indices;
         p.status = ds->status;
-        return launch<fp8g::FORM_GROUPED, __nv_bfloat16>(*ds, 2, map_a, map_b, p, tiles, stream);
+        return launch<fp8g::FORM_GROUPED, __nv_bfloat16, false>(*ds, 2, map_a, map_b, p, tiles, stream);
     } catch (...) {
         return fail(FP8G_ERR_CUDA, "unexpected exception");
     }
@@ -325,7 +369,7 @@ fp8g_status_t fp8_batch_gemm_masked(const void* a, const void* b, const float* a
         p.num_groups = static_cast<int>(num_groups);
         p.masked_m = masked_m;
         p.status = ds->status;
-        return launch<fp8g::FORM_MASKED, __nv_bfloat16>(*ds, 3, map_a, map_b, p, tiles, stream);
+        return launch<fp8g::FORM_MASKED, __nv_bfloat16, false>(*ds, 3, map_a, map_b, p, tiles, stream);
     } catch (...) {
         return fail(FP8G_ERR_CUDA, "unexpected exception");
     }

@@ -5,10 +5,10 @@
 //   out[i][j] = sum_kb P(i,j,kb) * a_scale(i,kb) * b_scale(j/128,kb),
 //   P(i,j,kb) = sum over the 128 k of block kb of a[i][k] * b[j][k].
 //
-// One CTA per SM walks output tiles of 128 x 256.  Per tile and per 128-wide
-// K block (one scale block):
-//   warp 0      TMA producer: loads the A (128x128) and B (256x128) E4M3 tiles
-//               into a 4-stage ring of 128-byte-swizzled shared-memory slots.
+// Each CTA owns 128 output rows x 256 columns of a tile at a time.  Per tile
+// and per 128-wide K block (one scale block):
+//   warp 0      TMA producer: loads this CTA's E4M3 tiles of A and B into a ring
+//               of 128-byte-swizzled shared-memory slots.
 //   warp 1      MMA issuer: 4 x tcgen05.mma (K = 32) write the block's partial
 //               sums P into one of two TMEM buffers (FP32, 128 lanes x 256 cols),
 //               fresh for every K block.
@@ -22,6 +22,18 @@
 // (setmaxnreg: 40 + 2 x 232 per thread, exactly the launch's 3 x 168).
 // The two TMEM buffers let the tensor cores compute block kb+1 while block kb
 // is being promoted, and the next tile's first blocks while the epilogue runs.
+//
+// Two variants of the pipeline:
+//   single CTA  (PAIR = false): a 128 x 256 tile per CTA; the producer loads
+//               A 128x128 and B 256x128 (48 KB) per K block into 4 slots.
+//   CTA pair    (PAIR = true, dense form): a cluster of two CTAs computes a
+//               256 x 256 tile with tcgen05.mma.cta_group::2 (M = 256).  Each
+//               CTA loads its own 128 rows of A and its half (128 rows) of B,
+//               32 KB per K block into 6 slots, so every SM moves a third less
+//               data through L2 and shared memory per MMA.  The even CTA issues
+//               the MMAs and multicasts their completion to both CTAs; the odd
+//               CTA's MMA warp relays "my slot has landed" to the even CTA, and
+//               its promotion warps release TMEM buffers on the even CTA.
 //
 // Every wait on a pipeline barrier is bounded: past the limit the waiting warp
 // raises an abort flag shared by the CTA and a bit in the device status word,
@@ -39,11 +51,10 @@
 
 namespace fp8g {
 
-constexpr int BLOCK_M = 128;  // tile rows = TMEM lanes = UMMA M
+constexpr int BLOCK_M = 128;  // rows per CTA = TMEM lanes
 constexpr int BLOCK_N = 256;  // tile columns = UMMA N
 constexpr int BLOCK_K = 128;  // one scale block along k = one 128-byte swizzle row of E4M3
 constexpr int UMMA_K = 32;    // K of one kind::f8f6f4 instruction
-constexpr int STAGES = 4;
 constexpr int NUM_PROMO_WARPS = 8;
 constexpr int FIRST_PROMO_WARP = 4;
 constexpr int NUM_THREADS = 128 + 32 * NUM_PROMO_WARPS;  // 3 warpgroups
@@ -52,14 +63,25 @@ constexpr uint32_t CONTROL_REGS = 40;   // warpgroup 0 after setmaxnreg.dec
 constexpr uint32_t PROMO_REGS = 232;    // warpgroups 1-2 after setmaxnreg.inc
 static_assert(128 * CONTROL_REGS + 256 * PROMO_REGS <= NUM_THREADS * LAUNCH_REGS,
               "register split exceeds the launch's registers");
-constexpr int A_TILE_BYTES = BLOCK_M * BLOCK_K;
-constexpr int B_TILE_BYTES = BLOCK_N * BLOCK_K;
 constexpr uint32_t TMEM_COLS = 2 * BLOCK_N;  // two FP32 partial buffers
 constexpr int BAR_BYTES = 256;               // barriers, TMEM slot, abort flag
-constexpr size_t SMEM_BYTES = 1024 /* alignment slack */ +
-                              size_t(STAGES) * (A_TILE_BYTES + B_TILE_BYTES) + BAR_BYTES;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
+constexpr uint64_t ABORT_GRACE_NS = 5000000ull;  // 5 ms
+
+// Geometry of the two pipeline variants.
+template <bool PAIR>
+struct Cfg {
+    static constexpr int TILE_M = PAIR ? 2 * BLOCK_M : BLOCK_M;  // rows of a scheduled tile
+    static constexpr int B_ROWS = PAIR ? BLOCK_N / 2 : BLOCK_N;  // B rows one CTA loads
+    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int A_BYTES = BLOCK_M * BLOCK_K;
+    static constexpr int B_BYTES = B_ROWS * BLOCK_K;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr size_t SMEM_BYTES = 1024 /* alignment slack */ +
+                                         size_t(STAGES) * STAGE_BYTES + BAR_BYTES;
+    static constexpr uint32_t IDESC = idesc_e4m3_f32(TILE_M, BLOCK_N);
+};
 
 enum Form { FORM_DENSE = 0, FORM_GROUPED = 1, FORM_MASKED = 2 };
 
@@ -74,32 +96,49 @@ struct Params {
     int n, k;
     int kblocks, nblocks;  // k/128, n/128
     int n_tiles;           // ceil(n / BLOCK_N)
-    int m_blocks;          // ceil(rows / BLOCK_M)
+    int m_blocks;          // ceil(rows / TILE_M)
     int num_tiles;         // dense/grouped: m_blocks * n_tiles
     int num_groups;
     int scale_mn_major;  // dense form only
     int band_m;          // m-blocks per raster band (dense/grouped)
 };
 
-// One output tile as every role sees it.
+// One output tile as every role of one CTA sees it.
 struct Tile {
-    int mb, nb;          // 128-row block (within the group for the masked form), 256-col block
+    int mb, nb;          // m-block (within the group for the masked form), 256-col block
     int group;           // expert (grouped) or group (masked); 0 for dense
-    int a_row0, b_row0;  // first row of the tile in the 2-D views of a and b
+    int row0;            // first of this CTA's 128 rows in the 2-D view of a (and out)
+    int b_row0;          // first row of b this CTA loads
     int group_rows;      // masked: valid rows of the group
     int row_expert[4];   // grouped: m_indices of rows 32q + lane, q = 0..3
     bool skip;           // grouped: padding-only block or broken precondition
 };
 
-// Maps tile ids to tiles.  All roles walk the same ids (blockIdx.x, +gridDim.x,
-// ...) through identical schedulers, so they agree on every tile.  Called by
-// whole warps (the grouped form reduces over the warp).
-template <int FORM>
+// Tile ids this CTA (or CTA pair) walks: first, first + stride, ...
+template <bool PAIR>
+__device__ __forceinline__ int tile_first() {
+    if constexpr (PAIR) return static_cast<int>(cluster_id_x());
+    return static_cast<int>(blockIdx.x);
+}
+template <bool PAIR>
+__device__ __forceinline__ int tile_stride() {
+    if constexpr (PAIR) return static_cast<int>(cluster_count_x());
+    return static_cast<int>(gridDim.x);
+}
+
+// Maps tile ids to tiles.  All roles walk the same ids through identical
+// schedulers, so they agree on every tile.  Called by whole warps (the grouped
+// form reduces over the warp).  `rank` is the CTA's rank in its pair (0 for a
+// single CTA).
+template <int FORM, bool PAIR>
 struct Scheduler {
+    using C = Cfg<PAIR>;
+    static_assert(!PAIR || FORM == FORM_DENSE, "CTA pairs serve the dense form");
     const Params& p;
+    const int rank;
     int g = 0;     // masked: group the cursor is in
     int base = 0;  // masked: first tile id of group g
-    __device__ explicit Scheduler(const Params& params) : p(params) {}
+    __device__ Scheduler(const Params& params, int cta_rank) : p(params), rank(cta_rank) {}
 
     __device__ int masked_rows(int grp, bool flag) const {
         const int v = __ldg(p.masked_m + grp);
@@ -137,7 +176,7 @@ struct Scheduler {
                     tile.mb = local - tile.nb * mbk;
                     tile.group = g;
                     tile.group_rows = rows_g;
-                    tile.a_row0 = g * p.rows + tile.mb * BLOCK_M;
+                    tile.row0 = g * p.rows + tile.mb * BLOCK_M;
                     tile.b_row0 = g * p.n + tile.nb * BLOCK_N;
                     return true;
                 }
@@ -148,14 +187,14 @@ struct Scheduler {
         } else {
             if (t >= p.num_tiles) return false;
             raster(t, tile.mb, tile.nb);
-            tile.a_row0 = tile.mb * BLOCK_M;
-            tile.b_row0 = tile.nb * BLOCK_N;
+            tile.row0 = tile.mb * C::TILE_M + rank * BLOCK_M;
+            tile.b_row0 = tile.nb * BLOCK_N + rank * C::B_ROWS;
             if constexpr (FORM == FORM_GROUPED) {
                 const int lane = threadIdx.x & 31;
                 int lo = INT_MAX, hi = -1, bad = 0;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const int row = tile.a_row0 + q * 32 + lane;
+                    const int row = tile.row0 + q * 32 + lane;
                     const int e = row < p.rows ? __ldg(p.m_indices + row) : -1;
                     tile.row_expert[q] = e;
                     if (e < -1 || e >= p.num_groups) {
@@ -183,12 +222,16 @@ struct Scheduler {
 };
 
 struct Ctl {
-    volatile int* abort_flag;
+    volatile int* abort_flag;  // this CTA's
+    uint32_t peer_abort;       // the other CTA's flag in the cluster window (pairs), else 0
     unsigned int* status;
 };
 
 // Wait for the phase of `bar` with the given parity; false if the CTA aborted
-// or this wait exceeded its limit (which aborts the CTA).
+// or this wait exceeded its limit (which aborts this CTA and, in a pair, the
+// other CTA too).  The phases are completed by tcgen05 commits, TMA
+// transactions or arrivals that follow completed tensor-memory reads, so the
+// default (CTA-scope) acquire of try_wait suffices also for pairs.
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const Ctl& c) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
@@ -198,6 +241,7 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const
             if (*c.abort_flag) return false;
             if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
                 *c.abort_flag = 1;
+                if (c.peer_abort) st_shared_remote(c.peer_abort, 1u);
                 atomicOr(c.status, FP8G_DEVICE_TIMEOUT);
                 return false;
             }
@@ -218,98 +262,160 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
         if (global_timer_ns() - t0 > DRAIN_LIMIT_NS) break;
 }
 
-template <int FORM>
+// After an abort, give asynchronous work still in flight (copies, MMAs and
+// the barrier arrivals they trigger) time to land before shared and tensor
+// memory are released.
+__device__ __forceinline__ void abort_grace() {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < ABORT_GRACE_NS) {
+    }
+}
+
+// The control roles below keep their per-K-block work on one thread (lane 0):
+// a K block is a handful of barrier polls, copies or MMAs, and anything the
+// whole warp does in that loop (converging, voting) delays the next MMA.  The
+// warp only acts together per tile, where the grouped scheduler needs it.
+
+template <int FORM, bool PAIR>
 __device__ __forceinline__ void run_producer(const CUtensorMap* map_a, const CUtensorMap* map_b,
-                                             const Params& p, uint8_t* sA, uint8_t* sB,
+                                             const Params& p, int rank, uint8_t* sA, uint8_t* sB,
                                              uint64_t* full, uint64_t* empty, const Ctl& ctl) {
+    using C = Cfg<PAIR>;
     const int lane = threadIdx.x & 31;
-    Scheduler<FORM> sched(p);
+    Scheduler<FORM, PAIR> sched(p, rank);
     int stage = 0;
     uint32_t phase = 0, armed = 0, armed_parity = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok; t += gridDim.x) {
+    for (int t = tile_first<PAIR>(); ok; t += tile_stride<PAIR>()) {
         Tile tile;
         if (!sched.next(t, tile, lane == 0)) break;
         if (tile.skip) continue;
-        for (int kb = 0; kb < p.kblocks; ++kb) {
-            if (!warp_wait(empty + stage, phase ^ 1u, ctl)) {
-                ok = false;
-                break;
-            }
-            if (lane == 0) {
-                mbar_arrive_expect_tx(full + stage, A_TILE_BYTES + B_TILE_BYTES);
-                tma_load_2d(sA + stage * A_TILE_BYTES, map_a, full + stage, kb * BLOCK_K,
-                            tile.a_row0);
-                tma_load_2d(sB + stage * B_TILE_BYTES, map_b, full + stage, kb * BLOCK_K,
+        if (lane == 0) {
+            for (int kb = 0; kb < p.kblocks; ++kb) {
+                if (!wait_phase(empty + stage, phase ^ 1u, ctl)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(full + stage, C::STAGE_BYTES);
+                tma_load_2d(sA + stage * C::A_BYTES, map_a, full + stage, kb * BLOCK_K, tile.row0);
+                tma_load_2d(sB + stage * C::B_BYTES, map_b, full + stage, kb * BLOCK_K,
                             tile.b_row0);
-            }
-            armed |= 1u << stage;
-            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-            __syncwarp();
-            if (++stage == STAGES) {
-                stage = 0;
-                phase ^= 1u;
+                armed |= 1u << stage;
+                armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
     }
-    // Every copy issued must have landed before shared memory is released.
+    // Every copy issued must have landed before shared memory is released.  (In
+    // the even CTA of a pair the phase also needs the odd CTA's relay, which has
+    // arrived whenever the pipeline ran to its end.)
     if (lane == 0)
-        for (int s = 0; s < STAGES; ++s)
+        for (int s = 0; s < C::STAGES; ++s)
             if ((armed >> s) & 1u) drain_wait(full + s, (armed_parity >> s) & 1u);
     __syncwarp();
 }
 
-template <int FORM>
+// MMA issuer of a single CTA, or of the even CTA of a pair.
+template <int FORM, bool PAIR>
 __device__ __forceinline__ void run_mma(const Params& p, uint8_t* sA, uint8_t* sB, uint64_t* full,
                                         uint64_t* empty, uint64_t* acc_full, uint64_t* acc_empty,
                                         uint64_t* drain, uint32_t tmem_base, const Ctl& ctl) {
+    using C = Cfg<PAIR>;
     const int lane = threadIdx.x & 31;
-    constexpr uint32_t IDESC = idesc_e4m3_f32(BLOCK_M, BLOCK_N);
-    Scheduler<FORM> sched(p);
+    Scheduler<FORM, PAIR> sched(p, 0);
+    // descriptors of slot 0; slot s is 16-byte units further on
+    const uint64_t a_desc0 = smem_desc_k_sw128(smem_u32(sA));
+    const uint64_t b_desc0 = smem_desc_k_sw128(smem_u32(sB));
     int stage = 0, buf = 0;
     uint32_t phase = 0, bphase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok; t += gridDim.x) {
+    for (int t = tile_first<PAIR>(); ok; t += tile_stride<PAIR>()) {
         Tile tile;
         if (!sched.next(t, tile, false)) break;
         if (tile.skip) continue;
-        for (int kb = 0; kb < p.kblocks; ++kb) {
-            if (!warp_wait(acc_empty + buf, bphase ^ 1u, ctl) ||
-                !warp_wait(full + stage, phase, ctl)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            if (lane == 0) {
+        if (lane == 0) {
+            for (int kb = 0; kb < p.kblocks; ++kb) {
+                if (!wait_phase(acc_empty + buf, bphase ^ 1u, ctl) ||
+                    !wait_phase(full + stage, phase, ctl)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BLOCK_N);
-                const uint64_t ad = smem_desc_k_sw128(smem_u32(sA + stage * A_TILE_BYTES));
-                const uint64_t bd = smem_desc_k_sw128(smem_u32(sB + stage * B_TILE_BYTES));
+                const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * C::A_BYTES) >> 4);
+                const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * C::B_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < BLOCK_K / UMMA_K; ++kk) {
                     // advance the start address by kk * 32 bytes inside the swizzled rows
                     const uint64_t step = static_cast<uint64_t>((kk * UMMA_K) >> 4);
-                    umma_f8f6f4(d, ad + step, bd + step, IDESC, kk > 0 ? 1u : 0u);
+                    if constexpr (PAIR)
+                        umma_f8f6f4_pair(d, ad + step, bd + step, C::IDESC, kk > 0 ? 1u : 0u);
+                    else
+                        umma_f8f6f4(d, ad + step, bd + step, C::IDESC, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(empty + stage);   // smem slot free once these MMAs finish
-                umma_commit(acc_full + buf);  // partial ready for promotion
-            }
-            __syncwarp();
-            if (++stage == STAGES) {
-                stage = 0;
-                phase ^= 1u;
-            }
-            if (++buf == 2) {
-                buf = 0;
-                bphase ^= 1u;
+                if constexpr (PAIR) {
+                    umma_commit_pair_multicast(empty + stage, 0x3);   // both CTAs' slots free
+                    umma_commit_pair_multicast(acc_full + buf, 0x3);  // both halves ready
+                } else {
+                    umma_commit(empty + stage);   // smem slot free once these MMAs finish
+                    umma_commit(acc_full + buf);  // partial ready for promotion
+                }
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                buf ^= 1;
+                bphase ^= static_cast<uint32_t>(buf == 0);
             }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
     }
     // All MMAs issued must have completed before TMEM and shared memory go away.
     if (lane == 0) {
-        umma_commit(drain);
+        if constexpr (PAIR)
+            umma_commit_pair(drain);
+        else
+            umma_commit(drain);
         drain_wait(drain, 0);
     }
     __syncwarp();
+}
+
+// Odd CTA of a pair: tell the even CTA each time one of this CTA's slots has
+// landed, so that its MMA warp sees both halves of a stage on one barrier.
+template <int FORM>
+__device__ __forceinline__ void run_relay(const Params& p, uint64_t* full, const Ctl& ctl) {
+    using C = Cfg<true>;
+    const int lane = threadIdx.x & 31;
+    Scheduler<FORM, true> sched(p, 1);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    uint32_t remote_full[C::STAGES];
+#pragma unroll
+    for (int s = 0; s < C::STAGES; ++s) remote_full[s] = mapa_shared(full + s, 0);
+    for (int t = tile_first<true>(); ok; t += tile_stride<true>()) {
+        Tile tile;
+        if (!sched.next(t, tile, false)) break;
+        if (lane == 0) {
+            for (int kb = 0; kb < p.kblocks; ++kb) {
+                if (!wait_phase(full + stage, phase, ctl)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_remote(remote_full[stage]);
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16*) {
@@ -344,8 +450,8 @@ __device__ __forceinline__ float load_scale(const float* sa, int sa_step, const 
     return x * y;
 }
 
-template <int FORM, typename OutT>
-__device__ __forceinline__ void run_promotion(const Params& p, uint64_t* acc_full,
+template <int FORM, typename OutT, bool PAIR>
+__device__ __forceinline__ void run_promotion(const Params& p, int rank, uint64_t* acc_full,
                                               uint64_t* acc_empty, uint32_t tmem_base,
                                               const Ctl& ctl) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -354,10 +460,16 @@ __device__ __forceinline__ void run_promotion(const Params& p, uint64_t* acc_ful
     const int r = quarter * 32 + lane;  // row of the tile owned by this thread
     const int KB = p.kblocks;
     OutT* out = static_cast<OutT*>(p.out);
-    Scheduler<FORM> sched(p);
+    Scheduler<FORM, PAIR> sched(p, rank);
+    // A pair's TMEM buffers are released on the even CTA, whose MMA warp reuses them.
+    uint32_t release0 = 0, release1 = 0;
+    if constexpr (PAIR) {
+        release0 = mapa_shared(acc_empty + 0, 0);
+        release1 = mapa_shared(acc_empty + 1, 0);
+    }
     int buf = 0;
     uint32_t bphase = 0;
-    for (int t = blockIdx.x;; t += gridDim.x) {
+    for (int t = tile_first<PAIR>();; t += tile_stride<PAIR>()) {
         Tile tile;
         if (!sched.next(t, tile, false)) break;
         if (tile.skip) continue;
@@ -376,7 +488,7 @@ __device__ __forceinline__ void run_promotion(const Params& p, uint64_t* acc_ful
             if (rin < p.rows) sa = p.a_scale + out_row * KB;
             if (col_ok) sb = p.b_scale + (static_cast<int64_t>(tile.group) * p.nblocks + jb) * KB;
         } else {
-            out_row = static_cast<int64_t>(tile.mb) * BLOCK_M + r;
+            out_row = static_cast<int64_t>(tile.row0) + r;
             const bool row_in = out_row < p.rows;
             if constexpr (FORM == FORM_GROUPED) {
                 row_ok = row_in && tile.row_expert[quarter] == tile.group;
@@ -411,17 +523,36 @@ __device__ __forceinline__ void run_promotion(const Params& p, uint64_t* acc_ful
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(buf * BLOCK_N + half * 128);
             const uint64_t s2 = splat2(s);
+            // Eight 16-column chunks; the load of chunk c+1 is in flight while
+            // chunk c is accumulated.
+            uint32_t va[16], vb[16];
+            tmem_load_16cols_async(taddr, va);
+            tmem_wait_16(va);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t v[64];
-                tmem_load_64cols(taddr + c * 64, v);
+            for (int c = 0; c < 8; c += 2) {
+                tmem_load_16cols_async(taddr + (c + 1) * 16, vb);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    acc[c * 32 + i] = ffma2(v[2 * i], v[2 * i + 1], s2, acc[c * 32 + i]);
+                for (int i = 0; i < 8; ++i)
+                    acc[c * 8 + i] = ffma2(va[2 * i], va[2 * i + 1], s2, acc[c * 8 + i]);
+                tmem_wait_16(vb);
+                if (c + 2 < 8) {
+                    tmem_load_16cols_async(taddr + (c + 2) * 16, va);
+                } else {
+                    // the whole partial is in registers: hand the buffer back first
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (PAIR)
+                            mbar_arrive_remote(buf == 0 ? release0 : release1);
+                        else
+                            mbar_arrive(acc_empty + buf);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    acc[(c + 1) * 8 + i] = ffma2(vb[2 * i], vb[2 * i + 1], s2, acc[(c + 1) * 8 + i]);
+                if (c + 2 < 8) tmem_wait_16(va);
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty + buf);
             if (++buf == 2) {
                 buf = 0;
                 bphase ^= 1u;
@@ -432,32 +563,35 @@ __device__ __forceinline__ void run_promotion(const Params& p, uint64_t* acc_ful
     }
 }
 
-template <int FORM, typename OutT>
+template <int FORM, typename OutT, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const Params p) {
+    using C = Cfg<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
-    uint8_t* sB = smem + STAGES * A_TILE_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_TILE_BYTES);
-    uint64_t* empty = full + STAGES;
-    uint64_t* acc_full = empty + STAGES;
+    uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* acc_full = empty + C::STAGES;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
+    const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full + s, 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            // the even CTA of a pair also counts the odd CTA's relay
+            mbar_init(full + s, (PAIR && rank == 0) ? 2 : 1);
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full + b, 1);
-            mbar_init(acc_empty + b, NUM_PROMO_WARPS);
+            mbar_init(acc_empty + b, PAIR ? 2 * NUM_PROMO_WARPS : NUM_PROMO_WARPS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -468,31 +602,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_map(&map_b);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(tmem_slot, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+    else
+        __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-    const Ctl ctl{abort_flag, p.status};
+    const Ctl ctl{abort_flag, PAIR ? mapa_shared(abort_flag, rank ^ 1) : 0u, p.status};
 
     if (warp < FIRST_PROMO_WARP) {
         regs_dec<CONTROL_REGS>();
-        if (warp == 0)
-            run_producer<FORM>(&map_a, &map_b, p, sA, sB, full, empty, ctl);
-        else if (warp == 1)
-            run_mma<FORM>(p, sA, sB, full, empty, acc_full, acc_empty, drain, tmem_base, ctl);
+        if (warp == 0) {
+            run_producer<FORM, PAIR>(&map_a, &map_b, p, rank, sA, sB, full, empty, ctl);
+        } else if (warp == 1) {
+            if constexpr (PAIR) {
+                if (rank == 0)
+                    run_mma<FORM, true>(p, sA, sB, full, empty, acc_full, acc_empty, drain,
+                                        tmem_base, ctl);
+                else
+                    run_relay<FORM>(p, full, ctl);
+            } else {
+                run_mma<FORM, false>(p, sA, sB, full, empty, acc_full, acc_empty, drain, tmem_base,
+                                     ctl);
+            }
+        }
     } else {
         regs_inc<PROMO_REGS>();
-        run_promotion<FORM, OutT>(p, acc_full, acc_empty, tmem_base, ctl);
+        run_promotion<FORM, OutT, PAIR>(p, rank, acc_full, acc_empty, tmem_base, ctl);
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync();  // no CTA leaves while the other may still signal it
+    else
+        __syncthreads();
+    if (*reinterpret_cast<volatile int*>(abort_flag)) {
+        abort_grace();
+        if constexpr (PAIR)
+            cluster_sync();
+        else
+            __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 

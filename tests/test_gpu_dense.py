@@ -38,23 +38,25 @@ def test_small_workload_full_parity(fp8g, oracle_mod):
     assert np.mean(bits16(out) == bits) > 0.5
 
 
+@pytest.mark.parametrize("mma_sm", [1, 2])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("major", ["K", "MN"])
 @pytest.mark.parametrize("mnk", [(200, 384, 384), (1, 128, 128), (7, 256, 640), (129, 640, 256),
-                                 (384, 512, 1152)])
-def test_ragged_shapes_full_parity(fp8g, oracle_mod, mnk, major, out_dtype):
+                                 (384, 512, 1152), (520, 384, 256)])
+def test_ragged_shapes_full_parity(fp8g, oracle_mod, mnk, major, out_dtype, mma_sm):
     m, n, k = mnk
     w = workloads.dense(m, n, k, seed=m * 7 + n + k, scale_major=major)
-    out = _run(fp8g, w, out_dtype)
+    out = _run(fp8g, w, out_dtype, mma_sm=mma_sm)
     ref, _ = _oracle_full(oracle_mod, w, out_dtype)
     assert written_rows(out).all()
     assert_close(as_f64(out), ref, "dense %s %s" % (mnk, major))
 
 
-def test_multi_wave_full_parity(fp8g, oracle_mod):
-    # more tiles than SMs, several K blocks, m and n tails
+@pytest.mark.parametrize("mma_sm", [1, 2])
+def test_multi_wave_full_parity(fp8g, oracle_mod, mma_sm):
+    # more tiles than SMs (or SM pairs), several K blocks, m and n tails
     w = workloads.dense(2100, 2432, 512, seed=77)
-    out = _run(fp8g, w)
+    out = _run(fp8g, w, mma_sm=mma_sm)
     ref, _ = _oracle_full(oracle_mod, w, torch.bfloat16)
     assert_close(as_f64(out), ref, "dense 2100x2432x512")
 
@@ -62,7 +64,7 @@ def test_multi_wave_full_parity(fp8g, oracle_mod):
 @pytest.mark.parametrize("major", ["K", "MN"])
 def test_dense_4096x7168x2048_sampled(fp8g, oracle_mod, major):
     w = workloads.make("dense_4096x7168x2048", scale_major=major)
-    out = _run(fp8g, w)
+    out = _run(fp8g, w, mma_sm=0)  # the launch configuration bench.py times
     assert written_rows(out).all()
     r, c = workloads.sample_positions(w["m"], w["n"], 65536, seed=11, extra_rows=(0, w["m"] - 1))
     sm = oracle_mod.SCALE_MN_MAJOR if major == "MN" else oracle_mod.SCALE_K_MAJOR
@@ -74,7 +76,7 @@ def test_dense_4096x7168x2048_sampled(fp8g, oracle_mod, major):
 def test_dense_16384x18432x7168_f16_sampled(fp8g, oracle_mod):
     w = workloads.make("dense_16384x18432x7168", device="cuda")
     out = torch.empty((w["m"], w["n"]), dtype=torch.float16, device="cuda")
-    fp8g.fp8_gemm_nt_groupwise(w["a"], w["b"], w["a_scale"], w["b_scale"], out)
+    fp8g.fp8_gemm_nt_groupwise(w["a"], w["b"], w["a_scale"], w["b_scale"], out, mma_sm=0)
     torch.cuda.synchronize()
     r, c = workloads.sample_positions(w["m"], w["n"], 65536, seed=12, extra_rows=(0, w["m"] - 1))
     host = {k: w[k].cpu() for k in ("a", "b", "a_scale", "b_scale")}
@@ -123,9 +125,30 @@ def test_layout_equivalence_bit_exact(fp8g):
 
 
 @pytest.mark.parametrize("mma_sm", [0, 2])
-def test_mma_sm_hint_does_not_change_results(fp8g, mma_sm):
-    w = workloads.dense(333, 640, 512, seed=92)
+@pytest.mark.parametrize("mnk", [(333, 640, 512), (4096, 2048, 1024)])
+def test_mma_sm_hint_does_not_change_results(fp8g, mma_sm, mnk):
+    w = workloads.dense(*mnk, seed=92)
     assert np.array_equal(bits16(_run(fp8g, w, mma_sm=1)), bits16(_run(fp8g, w, mma_sm=mma_sm)))
+
+
+def test_cta_pair_all_ones_and_doubling_exact(fp8g):
+    m, n, k = 512, 512, 384
+    a = torch.full((m, k), 0x38, dtype=torch.uint8)
+    b = torch.full((n, k), 0x38, dtype=torch.uint8)
+    g = torch.Generator().manual_seed(6)
+    ea = torch.randint(-4, 3, (m, k // 128), generator=g).float()
+    eb = torch.randint(-4, 3, (n // 128, k // 128), generator=g).float()
+    w = dict(a=a, b=b, a_scale=torch.exp2(ea), b_scale=torch.exp2(eb), m=m, n=n, k=k,
+             scale_major="K")
+    out = _run(fp8g, w, mma_sm=2)
+    want = (128.0 * torch.exp2(ea)[:, None, :] * torch.exp2(eb).repeat_interleave(128, 0)[None]).sum(-1)
+    assert torch.equal(out.float().cpu(), want.to(torch.bfloat16).float())
+    w2 = dict(w, a_scale=w["a_scale"].clone())
+    w2["a_scale"][300] *= 2.0  # a row of the odd CTA of a pair
+    out2 = _run(fp8g, w2, mma_sm=2)
+    expect = out.float().cpu().clone()
+    expect[300] *= 2.0
+    assert torch.equal(out2.float().cpu(), expect)
 
 
 def test_deterministic_and_side_stream(fp8g):
