@@ -151,7 +151,7 @@ fp8g_status_t check_ptrs(const void* a, const void* b, const float* a_scale, con
 template <int FORM, typename OutT, bool PAIR>
 fp8g_status_t launch(DeviceState& ds, int slot, const CUtensorMap& map_a, const CUtensorMap& map_b,
                      const Params& p, int64_t max_tiles, cudaStream_t stream) {
-    using C = fp8g::Cfg<PAIR>;
+    using C = fp8g::Cfg<PAIR, FORM>;
     auto kernel = fp8g::gemm_kernel<FORM, OutT, PAIR>;
     cudaLaunchAttribute cluster_attr;
     cluster_attr.id = cudaLaunchAttributeClusterDimension;

@@ -9,14 +9,15 @@
 // and per 128-wide K block (one scale block):
 //   warp 0      TMA producer: loads this CTA's E4M3 tiles of A and B into a ring
 //               of 128-byte-swizzled shared-memory slots.
-//   warp 1      MMA issuer: 4 x tcgen05.mma (K = 32) write the block's partial
-//               sums P into one of two TMEM buffers (FP32, 128 lanes x 256 cols),
-//               fresh for every K block.
-//   warps 2-3   idle (they complete the first warpgroup).
+//   warps 1-2   MMA issuers (even / odd K blocks): 4 x tcgen05.mma (K = 32)
+//               write the block's partial sums P into TMEM buffer 0 / 1 (FP32,
+//               128 lanes x 256 cols), fresh for every K block.
+//   warp 3      idle (it completes the first warpgroup).
 //   warps 4-11  promotion + epilogue: read the partial from TMEM, multiply by
 //               a_scale(row,kb) * b_scale(col block,kb) and accumulate in FP32
 //               registers (one row per thread, 128 columns per warpgroup);
-//               after the last K block convert to BF16/FP16 and store the row.
+//               after the last K block round to BF16/FP16 through a shared-memory
+//               staging slice and store whole 128-byte row segments.
 // The 128 x 256 FP32 running sums take half of the register file, so the
 // control warpgroup hands registers to the two promotion warpgroups
 // (setmaxnreg: 40 + 2 x 232 per thread, exactly the launch's 3 x 168).
@@ -25,11 +26,12 @@
 //
 // Two variants of the pipeline:
 //   single CTA  (PAIR = false): a 128 x 256 tile per CTA; the producer loads
-//               A 128x128 and B 256x128 (48 KB) per K block into 4 slots.
+//               A 128x128 and B 256x128 (48 KB) per K block into 3 slots (4
+//               for the masked form).
 //   CTA pair    (PAIR = true, dense form): a cluster of two CTAs computes a
 //               256 x 256 tile with tcgen05.mma.cta_group::2 (M = 256).  Each
 //               CTA loads its own 128 rows of A and its half (128 rows) of B,
-//               32 KB per K block into 6 slots, so every SM moves a third less
+//               32 KB per K block into 5 slots, so every SM moves a third less
 //               data through L2 and shared memory per MMA.  The even CTA issues
 //               the MMAs and multicasts their completion to both CTAs; the odd
 //               CTA's MMA warp relays "my slot has landed" to the even CTA, and
@@ -65,25 +67,33 @@ static_assert(128 * CONTROL_REGS + 256 * PROMO_REGS <= NUM_THREADS * LAUNCH_REGS
               "register split exceeds the launch's registers");
 constexpr uint32_t TMEM_COLS = 2 * BLOCK_N;  // two FP32 partial buffers
 constexpr int BAR_BYTES = 256;               // barriers, TMEM slot, abort flag
+// Output staging: each promotion warpgroup rounds 128 rows x 64 columns at a
+// time into 128-byte rows of shared memory before the warps store them.
+constexpr int OUT_COLS = 64;
+constexpr int OUT_STAGE_BYTES = BLOCK_M * OUT_COLS * 2;  // 16 KB per warpgroup
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
 constexpr uint64_t ABORT_GRACE_NS = 5000000ull;  // 5 ms
 
-// Geometry of the two pipeline variants.
-template <bool PAIR>
+enum Form { FORM_DENSE = 0, FORM_GROUPED = 1, FORM_MASKED = 2 };
+
+// Geometry of the pipeline variants.  Ring depths: shared memory left over
+// becomes L1, which the per-row scale loads of the promotion warps live on, so
+// the rings are as deep as the copies need and no deeper (measured); the
+// HBM-bound masked form keeps one more slot in flight.
+template <bool PAIR, int FORM>
 struct Cfg {
     static constexpr int TILE_M = PAIR ? 2 * BLOCK_M : BLOCK_M;  // rows of a scheduled tile
     static constexpr int B_ROWS = PAIR ? BLOCK_N / 2 : BLOCK_N;  // B rows one CTA loads
-    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int STAGES = PAIR ? 5 : (FORM == FORM_MASKED ? 4 : 3);
     static constexpr int A_BYTES = BLOCK_M * BLOCK_K;
     static constexpr int B_BYTES = B_ROWS * BLOCK_K;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr size_t SMEM_BYTES = 1024 /* alignment slack */ +
-                                         size_t(STAGES) * STAGE_BYTES + BAR_BYTES;
+                                         size_t(STAGES) * STAGE_BYTES + 2 * OUT_STAGE_BYTES +
+                                         BAR_BYTES;
     static constexpr uint32_t IDESC = idesc_e4m3_f32(TILE_M, BLOCK_N);
 };
-
-enum Form { FORM_DENSE = 0, FORM_GROUPED = 1, FORM_MASKED = 2 };
 
 struct Params {
     const float* a_scale;
@@ -132,7 +142,7 @@ __device__ __forceinline__ int tile_stride() {
 // single CTA).
 template <int FORM, bool PAIR>
 struct Scheduler {
-    using C = Cfg<PAIR>;
+    using C = Cfg<PAIR, FORM>;
     static_assert(!PAIR || FORM == FORM_DENSE, "CTA pairs serve the dense form");
     const Params& p;
     const int rank;
@@ -280,7 +290,7 @@ template <int FORM, bool PAIR>
 __device__ __forceinline__ void run_producer(const CUtensorMap* map_a, const CUtensorMap* map_b,
                                              const Params& p, int rank, uint8_t* sA, uint8_t* sB,
                                              uint64_t* full, uint64_t* empty, const Ctl& ctl) {
-    using C = Cfg<PAIR>;
+    using C = Cfg<PAIR, FORM>;
     const int lane = threadIdx.x & 31;
     Scheduler<FORM, PAIR> sched(p, rank);
     int stage = 0;
@@ -319,33 +329,44 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* map_a, const CUt
     __syncwarp();
 }
 
-// MMA issuer of a single CTA, or of the even CTA of a pair.
+// MMA issuers of a single CTA, or of the even CTA of a pair.  The tensor pipe
+// accepts an MMA only when the previous one is under way, so an issuing thread
+// is held for most of a K block.  Two warps therefore share the work: the warp
+// with `parity` 0 issues the even K blocks (TMEM buffer 0), parity 1 the odd
+// ones (buffer 1); while one is held issuing block j, the other has passed the
+// barriers of block j+1 and queues it right behind.  A commit tracks only its
+// own thread's MMAs, so each block is still signalled exactly when it is done.
 template <int FORM, bool PAIR>
 __device__ __forceinline__ void run_mma(const Params& p, uint8_t* sA, uint8_t* sB, uint64_t* full,
                                         uint64_t* empty, uint64_t* acc_full, uint64_t* acc_empty,
-                                        uint64_t* drain, uint32_t tmem_base, const Ctl& ctl) {
-    using C = Cfg<PAIR>;
+                                        uint64_t* drain, uint32_t tmem_base, const Ctl& ctl,
+                                        int parity) {
+    using C = Cfg<PAIR, FORM>;
     const int lane = threadIdx.x & 31;
     Scheduler<FORM, PAIR> sched(p, 0);
     // descriptors of slot 0; slot s is 16-byte units further on
     const uint64_t a_desc0 = smem_desc_k_sw128(smem_u32(sA));
     const uint64_t b_desc0 = smem_desc_k_sw128(smem_u32(sB));
-    int stage = 0, buf = 0;
-    uint32_t phase = 0, bphase = 0;
+    const int buf = parity;
+    const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BLOCK_N);
+    uint32_t j = 0;  // K blocks of this CTA's tiles so far, both parities
     bool ok = true;
     for (int t = tile_first<PAIR>(); ok; t += tile_stride<PAIR>()) {
         Tile tile;
         if (!sched.next(t, tile, false)) break;
         if (tile.skip) continue;
         if (lane == 0) {
-            for (int kb = 0; kb < p.kblocks; ++kb) {
+            for (int kb = 0; kb < p.kblocks; ++kb, ++j) {
+                if ((j & 1u) != static_cast<uint32_t>(parity)) continue;
+                const uint32_t stage = j % C::STAGES;
+                const uint32_t phase = (j / C::STAGES) & 1u;
+                const uint32_t bphase = (j >> 1) & 1u;
                 if (!wait_phase(acc_empty + buf, bphase ^ 1u, ctl) ||
                     !wait_phase(full + stage, phase, ctl)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BLOCK_N);
                 const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * C::A_BYTES) >> 4);
                 const uint64_t bd = b_desc0 + static_cast<uint64_t>((stage * C::B_BYTES) >> 4);
 #pragma unroll
@@ -364,17 +385,12 @@ __device__ __forceinline__ void run_mma(const Params& p, uint8_t* sA, uint8_t* s
                     umma_commit(empty + stage);   // smem slot free once these MMAs finish
                     umma_commit(acc_full + buf);  // partial ready for promotion
                 }
-                if (++stage == C::STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-                buf ^= 1;
-                bphase ^= static_cast<uint32_t>(buf == 0);
             }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
     }
-    // All MMAs issued must have completed before TMEM and shared memory go away.
+    // All MMAs issued must have completed before TMEM and shared memory go away
+    // (the drain barrier counts both issuing warps).
     if (lane == 0) {
         if constexpr (PAIR)
             umma_commit_pair(drain);
@@ -389,7 +405,7 @@ __device__ __forceinline__ void run_mma(const Params& p, uint8_t* sA, uint8_t* s
 // landed, so that its MMA warp sees both halves of a stage on one barrier.
 template <int FORM>
 __device__ __forceinline__ void run_relay(const Params& p, uint64_t* full, const Ctl& ctl) {
-    using C = Cfg<true>;
+    using C = Cfg<true, FORM>;
     const int lane = threadIdx.x & 31;
     Scheduler<FORM, true> sched(p, 1);
     int stage = 0;
@@ -427,19 +443,47 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, __half*) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// 128 consecutive outputs of one row (acc2[i] holds columns 2i, 2i+1),
-// 16-byte stores.
+// Epilogue of one promotion warpgroup: its 128 rows x 128 columns of FP32
+// sums (thread r holds row r; acc[i] = columns 2i, 2i+1) go out in two passes
+// of 64 columns.  Each thread rounds its row segment into 128 bytes of shared
+// memory (16-byte chunk c of row r at chunk c ^ (r % 8), so that the 32 rows
+// a warp writes at once spread over all banks); then each warp stores the 32
+// rows it owns as full 128-byte segments, four rows per instruction, skipping
+// rows outside the form.  `row_base` is the output row of tile row 0.
 template <typename OutT>
-__device__ __forceinline__ void store_row128(OutT* dst, const uint64_t (&acc2)[64]) {
+__device__ __forceinline__ void store_tile_rows(OutT* out, int64_t n, int64_t row_base, int col0,
+                                                bool row_ok, const uint64_t (&acc)[64],
+                                                uint8_t* staging, uint32_t barrier_id) {
+    const int lane = threadIdx.x & 31;
+    const int quarter = (threadIdx.x >> 5) & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t base = smem_u32(staging);
     OutT* tag = nullptr;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        uint4 v;
-        v.x = pack2(lo_f32(acc2[4 * i + 0]), hi_f32(acc2[4 * i + 0]), tag);
-        v.y = pack2(lo_f32(acc2[4 * i + 1]), hi_f32(acc2[4 * i + 1]), tag);
-        v.z = pack2(lo_f32(acc2[4 * i + 2]), hi_f32(acc2[4 * i + 2]), tag);
-        v.w = pack2(lo_f32(acc2[4 * i + 3]), hi_f32(acc2[4 * i + 3]), tag);
-        reinterpret_cast<uint4*>(dst)[i] = v;
+    for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int a = pass * 32 + 4 * c;
+            uint4 v;
+            v.x = pack2(lo_f32(acc[a + 0]), hi_f32(acc[a + 0]), tag);
+            v.y = pack2(lo_f32(acc[a + 1]), hi_f32(acc[a + 1]), tag);
+            v.z = pack2(lo_f32(acc[a + 2]), hi_f32(acc[a + 2]), tag);
+            v.w = pack2(lo_f32(acc[a + 3]), hi_f32(acc[a + 3]), tag);
+            st_shared_v4(base + r * 128 + ((c ^ (r & 7)) << 4), v);
+        }
+        named_barrier_sync(barrier_id, 128);
+        const int chunk = lane & 7;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int i = 4 * k + (lane >> 3);  // row within this warp's 32
+            const int rr = quarter * 32 + i;    // row within the tile
+            const bool ok_i = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, i) != 0;
+            const uint4 v = ld_shared_v4(base + rr * 128 + ((chunk ^ (rr & 7)) << 4));
+            if (ok_i)
+                *reinterpret_cast<uint4*>(out + (row_base + rr) * n + col0 + pass * OUT_COLS +
+                                          chunk * 8) = v;
+        }
+        named_barrier_sync(barrier_id, 128);  // staging free for the next pass
     }
 }
 
@@ -453,7 +497,7 @@ __device__ __forceinline__ float load_scale(const float* sa, int sa_step, const 
 template <int FORM, typename OutT, bool PAIR>
 __device__ __forceinline__ void run_promotion(const Params& p, int rank, uint64_t* acc_full,
                                               uint64_t* acc_empty, uint32_t tmem_base,
-                                              const Ctl& ctl) {
+                                              uint8_t* sOut, const Ctl& ctl) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quarter = warp & 3;       // this warp may read TMEM lanes 32*quarter .. +31
     const int half = (warp - FIRST_PROMO_WARP) >> 2;  // which 128 columns of the tile
@@ -558,8 +602,12 @@ __device__ __forceinline__ void run_promotion(const Params& p, int rank, uint64_
                 bphase ^= 1u;
             }
         }
-        if (!ok) break;
-        if (row_ok && col_ok) store_row128(out + out_row * p.n + col0, acc);
+        // Every warp of the warpgroup takes part in the epilogue's barriers, also
+        // after an abort (then storing nothing); the warpgroup stops together.
+        if (col_ok)  // uniform over the warpgroup
+            store_tile_rows<OutT>(out, p.n, out_row - r, col0, ok && row_ok, acc,
+                                  sOut + half * OUT_STAGE_BYTES, 1 + half);
+        if (named_barrier_or(1 + half, 128, !ok)) break;
     }
 }
 
@@ -567,13 +615,14 @@ template <int FORM, typename OutT, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                 const Params p) {
-    using C = Cfg<PAIR>;
+    using C = Cfg<PAIR, FORM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+    uint8_t* sOut = sB + C::STAGES * C::B_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 2 * OUT_STAGE_BYTES);
     uint64_t* empty = full + C::STAGES;
     uint64_t* acc_full = empty + C::STAGES;
     uint64_t* acc_empty = acc_full + 2;
@@ -593,7 +642,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(acc_full + b, 1);
             mbar_init(acc_empty + b, PAIR ? 2 * NUM_PROMO_WARPS : NUM_PROMO_WARPS);
         }
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);  // one commit from each MMA-issuing warp
         *abort_flag = 0;
         mbar_init_fence();
     }
@@ -623,21 +672,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         regs_dec<CONTROL_REGS>();
         if (warp == 0) {
             run_producer<FORM, PAIR>(&map_a, &map_b, p, rank, sA, sB, full, empty, ctl);
-        } else if (warp == 1) {
+        } else if (warp == 1 || warp == 2) {
             if constexpr (PAIR) {
-                if (rank == 0)
+                if (rank == 1) {
+                    if (warp == 1) run_relay<FORM>(p, full, ctl);
+                } else {
                     run_mma<FORM, true>(p, sA, sB, full, empty, acc_full, acc_empty, drain,
-                                        tmem_base, ctl);
-                else
-                    run_relay<FORM>(p, full, ctl);
+                                        tmem_base, ctl, warp - 1);
+                }
             } else {
                 run_mma<FORM, false>(p, sA, sB, full, empty, acc_full, acc_empty, drain, tmem_base,
-                                     ctl);
+                                     ctl, warp - 1);
             }
         }
     } else {
         regs_inc<PROMO_REGS>();
-        run_promotion<FORM, OutT, PAIR>(p, rank, acc_full, acc_empty, tmem_base, ctl);
+        run_promotion<FORM, OutT, PAIR>(p, rank, acc_full, acc_empty, tmem_base, sOut, ctl);
     }
 
     tc_fence_before_sync();
