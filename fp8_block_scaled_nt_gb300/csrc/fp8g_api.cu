@@ -153,19 +153,22 @@ fp8g_status_t launch(DeviceState& ds, int slot, const CUtensorMap& map_a, const 
                      const Params& p, int64_t max_tiles, cudaStream_t stream) {
     using C = fp8g::Cfg<PAIR, FORM>;
     auto kernel = fp8g::gemm_kernel<FORM, OutT, PAIR>;
-    cudaLaunchAttribute cluster_attr;
-    cluster_attr.id = cudaLaunchAttributeClusterDimension;
-    cluster_attr.val.clusterDim.x = 2;
-    cluster_attr.val.clusterDim.y = 1;
-    cluster_attr.val.clusterDim.z = 1;
+    // The kernel's prologue (barriers, TMEM, tensor-map prefetch) may overlap
+    // the previous kernel on the stream; it waits for that kernel's completion
+    // (griddepcontrol.wait) before touching global memory.
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = 2;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(fp8g::NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
-    if (PAIR) {
-        cfg.attrs = &cluster_attr;
-        cfg.numAttrs = 1;
-    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = PAIR ? 2 : 1;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!ds.kernel_ready[slot]) {
@@ -185,9 +188,12 @@ fp8g_status_t launch(DeviceState& ds, int slot, const CUtensorMap& map_a, const 
             int resident = ds.sm_count;
             if (PAIR) {
                 // persistent grid: as many CTA pairs as can be resident at once
-                cfg.gridDim = dim3(2, 1, 1);
+                cudaLaunchConfig_t occ = cfg;
+                occ.gridDim = dim3(2, 1, 1);
+                occ.attrs = &attrs[1];  // the cluster shape alone
+                occ.numAttrs = 1;
                 int clusters = 0;
-                e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+                e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &occ);
                 if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
                 if (clusters < 1)
                     return fail(FP8G_ERR_UNSUPPORTED, "no CTA pair of this kernel fits an SM pair");

@@ -487,11 +487,9 @@ __device__ __forceinline__ void store_tile_rows(OutT* out, int64_t n, int64_t ro
     }
 }
 
-__device__ __forceinline__ float load_scale(const float* sa, int sa_step, const float* sb,
-                                            int sb_step, int kb) {
-    const float x = sa ? __ldg(sa + static_cast<int64_t>(kb) * sa_step) : 0.0f;
-    const float y = sb ? __ldg(sb + static_cast<int64_t>(kb) * sb_step) : 0.0f;
-    return x * y;
+// One scale of K block kb (0 where the row or column block is outside the form).
+__device__ __forceinline__ float load_scale(const float* x, int step, int kb) {
+    return x ? __ldg(x + static_cast<int64_t>(kb) * step) : 0.0f;
 }
 
 template <int FORM, typename OutT, bool PAIR>
@@ -554,11 +552,17 @@ __device__ __forceinline__ void run_promotion(const Params& p, int rank, uint64_
         uint64_t acc[64];  // FP32 running sums, two columns per register pair
 #pragma unroll
         for (int i = 0; i < 64; ++i) acc[i] = 0;
-        float s_next = load_scale(sa, sa_step, sb, sb_step, 0);
+        // The scales of block kb+1 are loaded while block kb is processed and
+        // multiplied only when used, so that a miss in L1 (MN-major scales
+        // start a new line every K block) is not waited for early.
+        float xa = load_scale(sa, sa_step, 0), xb = load_scale(sb, sb_step, 0);
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb) {
-            const float s = s_next;
-            if (kb + 1 < KB) s_next = load_scale(sa, sa_step, sb, sb_step, kb + 1);
+            const float s = xa * xb;
+            if (kb + 1 < KB) {
+                xa = load_scale(sa, sa_step, kb + 1);
+                xb = load_scale(sb, sb_step, kb + 1);
+            }
             if (!warp_wait(acc_full + buf, bphase, ctl)) {
                 ok = false;
                 break;
@@ -667,6 +671,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
     const Ctl ctl{abort_flag, PAIR ? mapa_shared(abort_flag, rank ^ 1) : 0u, p.status};
+    // Everything above touches only this CTA's own resources, so it may overlap
+    // the tail of the previous kernel on the stream (launched with programmatic
+    // stream serialization); global memory is read and written only after it.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp < FIRST_PROMO_WARP) {
         regs_dec<CONTROL_REGS>();

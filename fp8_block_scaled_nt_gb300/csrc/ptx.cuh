@@ -49,6 +49,16 @@ __device__ __forceinline__ uint32_t cluster_count_x() {
 }
 
 // All threads of all CTAs of the cluster.
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible; allow the next dependent grid
+// on the stream to be scheduled.  Both are no-ops without such grids.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile(
         "barrier.cluster.arrive.release.aligned;\n\t"

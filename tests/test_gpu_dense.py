@@ -161,6 +161,31 @@ def test_deterministic_and_side_stream(fp8g):
     assert np.array_equal(first, bits16(second))
 
 
+def test_back_to_back_launches_keep_stream_order(fp8g):
+    # Each launch may start its prologue while the previous kernel on the stream
+    # is finishing; it must still read and write global memory only after it.
+    w1 = to_device(workloads.dense(640, 1024, 768, seed=96))
+    w2 = to_device(workloads.dense(640, 1024, 768, seed=97))
+    alone = sentinel_like((640, 1024), torch.bfloat16, "cuda")
+    fp8g.fp8_gemm_nt_groupwise(w2["a"], w2["b"], w2["a_scale"], w2["b_scale"], alone, mma_sm=2)
+    torch.cuda.synchronize()
+    out = sentinel_like((640, 1024), torch.bfloat16, "cuda")
+    for _ in range(3):
+        for w in (w1, w2):  # both write all of `out`; the second must win
+            fp8g.fp8_gemm_nt_groupwise(w["a"], w["b"], w["a_scale"], w["b_scale"], out, mma_sm=2)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits16(out), bits16(alone))
+    # an input rewritten between two launches is read in its new state
+    a = w1["a"].clone()
+    out1 = sentinel_like((640, 1024), torch.bfloat16, "cuda")
+    fp8g.fp8_gemm_nt_groupwise(a, w1["b"], w1["a_scale"], w1["b_scale"], out1, mma_sm=2)
+    a.copy_(w2["a"])
+    out2 = sentinel_like((640, 1024), torch.bfloat16, "cuda")
+    fp8g.fp8_gemm_nt_groupwise(a, w2["b"], w2["a_scale"], w2["b_scale"], out2, mma_sm=2)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits16(out2), bits16(alone))
+
+
 def test_empty_m(fp8g):
     a = torch.empty((0, 256), dtype=torch.uint8, device="cuda")
     b = torch.zeros((128, 256), dtype=torch.uint8, device="cuda")
