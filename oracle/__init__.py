@@ -7,7 +7,9 @@ the oracle, and the product path fails instead of falling back to it.
 The arithmetic lives in ``oracle.c`` (plain C, FP64, one rounding); this module
 only marshals numpy arrays (or CPU torch tensors) into it.  It follows the MATE
 page "FlashInfer Wrapper APIs", section GEMM: ``gemm_fp8_nt_groupwise``,
-``group_deepgemm_fp8_nt_groupwise`` and ``batch_deepgemm_fp8_nt_groupwise``.
+``group_deepgemm_fp8_nt_groupwise`` and ``batch_deepgemm_fp8_nt_groupwise``;
+and section Norm: ``fused_add_rmsnorm_fp8_block_quant`` (the producer of the
+GEMM's FP8 activations and their 1 x 128 scales).
 """
 import ctypes
 
@@ -45,7 +47,12 @@ def _load():
                                                  P, P, P]
         lib.oracle_batch_gemm_masked_at.argtypes = [P, P, P, P, P, I64, I64, I64, I64,
                                                     P, P, P, I64, P, P, P]
+        lib.oracle_e4m3_encode.argtypes = [P, I64, P]
+        lib.oracle_e4m3_encode.restype = None
+        lib.oracle_fused_add_rmsnorm_fp8_block_quant.argtypes = [
+            P, P, P, ctypes.c_double, I64, I64, P, P, P, P]
         for f in ("oracle_gemm_nt_groupwise", "oracle_gemm_nt_groupwise_at",
+                  "oracle_fused_add_rmsnorm_fp8_block_quant",
                   "oracle_group_gemm_contiguous", "oracle_group_gemm_contiguous_at",
                   "oracle_batch_gemm_masked", "oracle_batch_gemm_masked_at",
                   "oracle_num_threads"):
@@ -61,7 +68,11 @@ def _arr(x, dtype):
         if t.element_size() == 1 and dtype == np.uint8:
             import torch
             t = t.view(torch.uint8)
-        x = t.numpy()
+        if t.element_size() == 2 and dtype == np.uint16:  # BF16/FP16 encodings
+            import torch
+            x = t.view(torch.int16).numpy().view(np.uint16)
+        else:
+            x = t.numpy()
     a = np.ascontiguousarray(x)
     if a.dtype != dtype:
         if dtype == np.uint8:
@@ -205,3 +216,38 @@ def batch_gemm_masked_at(a, b, a_scale, b_scale, masked_m, groups, rows, cols):
         _p(rows), _p(cols), rows.size, _p(ref), _p(bits), _p(written))
     _check(rc, "batch_gemm_masked_at")
     return ref, bits, written.astype(bool)
+
+
+def e4m3_encode(x):
+    """E4M3 codes (uint8) of FP64 values: round to nearest even, saturate to
+    +-448, NaN -> 0x7F."""
+    x = _arr(x, np.float64)
+    codes = np.empty(x.shape, np.uint8)
+    _load().oracle_e4m3_encode(x.ctypes.data, x.size, codes.ctypes.data)
+    return codes
+
+
+def fused_add_rmsnorm_fp8_block_quant(input_bits, residual_bits, weight_bits, eps=1e-6):
+    """Fused add + RMSNorm + 1 x 128 FP8 quantisation of BF16 rows.
+
+    Arguments are the 16-bit encodings of BF16 tensors: input and residual
+    (rows, hidden), weight (hidden).  Returns a dict with ``residual_out`` and
+    ``normed_out`` (uint16 encodings, (rows, hidden)), ``out`` (E4M3 codes,
+    (rows, hidden)) and ``block_scale`` (float32, (rows, hidden // 128)).
+    """
+    x = _arr(input_bits, np.uint16)
+    r = _arr(residual_bits, np.uint16)
+    w = _arr(weight_bits, np.uint16)
+    rows, hidden = x.shape
+    if r.shape != x.shape or w.shape != (hidden,):
+        raise ValueError("shape mismatch")
+    res = dict(residual_out=np.empty((rows, hidden), np.uint16),
+               normed_out=np.empty((rows, hidden), np.uint16),
+               out=np.empty((rows, hidden), np.uint8),
+               block_scale=np.empty((rows, hidden // 128 if hidden % 128 == 0 else 0),
+                                    np.float32))
+    rc = _load().oracle_fused_add_rmsnorm_fp8_block_quant(
+        _p(x), _p(r), _p(w), float(eps), rows, hidden, _p(res["residual_out"]),
+        _p(res["normed_out"]), _p(res["out"]), _p(res["block_scale"]))
+    _check(rc, "fused_add_rmsnorm_fp8_block_quant")
+    return res

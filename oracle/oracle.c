@@ -450,3 +450,103 @@ int oracle_batch_gemm_masked_at(const uint8_t* a, const uint8_t* b,
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ E4M3 */
+
+#define E4M3_P 4
+#define E4M3_EMIN (-6)
+#define E4M3_MAX 448.0
+
+/* Code of a value already on the E4M3 grid with |y| <= 448. */
+static uint8_t e4m3_code_of(double y)
+{
+    uint8_t sign = signbit(y) ? 0x80 : 0;
+    double a = fabs(y);
+    if (a == 0.0)
+        return sign;
+    if (a < ldexp(1.0, E4M3_EMIN)) /* subnormal: a = f * 2^-9 */
+        return (uint8_t)(sign | (uint8_t)ldexp(a, 9));
+    int e2;
+    frexp(a, &e2);
+    int lead = e2 - 1; /* a = (1 + f/8) * 2^lead */
+    uint8_t f = (uint8_t)(ldexp(a, 3 - lead) - 8.0);
+    return (uint8_t)(sign | (uint8_t)((lead + 7) << 3) | f);
+}
+
+void oracle_e4m3_encode(const double* x, int64_t count, uint8_t* codes)
+{
+    for (int64_t s = 0; s < count; ++s) {
+        if (isnan(x[s])) {
+            codes[s] = 0x7F;
+            continue;
+        }
+        /* round on the grid; anything rounding past 448 saturates */
+        double y = round_to_format(x[s], E4M3_P, E4M3_EMIN, E4M3_MAX);
+        if (fabs(y) > E4M3_MAX)
+            y = copysign(E4M3_MAX, x[s]);
+        codes[s] = e4m3_code_of(y);
+    }
+}
+
+/* ------------------------------------------------- fused add RMSNorm + quant */
+
+static double bf16_value(uint16_t bits)
+{
+    union {
+        uint32_t u;
+        float f;
+    } v;
+    v.u = (uint32_t)bits << 16;
+    return (double)v.f;
+}
+
+int oracle_fused_add_rmsnorm_fp8_block_quant(const uint16_t* input,
+                                             const uint16_t* residual,
+                                             const uint16_t* weight, double eps,
+                                             int64_t rows, int64_t hidden,
+                                             uint16_t* residual_out,
+                                             uint16_t* normed_out, uint8_t* out,
+                                             float* block_scale)
+{
+    if (rows < 0 || hidden <= 0 || hidden % KBLOCK)
+        return -1;
+    const int64_t nblk = hidden / KBLOCK;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t i = 0; i < rows; ++i) {
+        const uint16_t* in = input + i * hidden;
+        const uint16_t* res = residual + i * hidden;
+        uint16_t* rout = residual_out + i * hidden;
+        uint16_t* nout = normed_out + i * hidden;
+        /* the sum of two BF16 values is exact in FP64; one rounding to BF16 */
+        double ss = 0.0;
+        for (int64_t j = 0; j < hidden; ++j) {
+            double x = round_one(bf16_value(in[j]) + bf16_value(res[j]),
+                                 ORACLE_OUT_BF16, &rout[j]);
+            ss += x * x;
+        }
+        double r = 1.0 / sqrt(ss / (double)hidden + eps);
+        for (int64_t j = 0; j < hidden; ++j) {
+            double x = bf16_value(rout[j]);
+            round_one(x * r * bf16_value(weight[j]), ORACLE_OUT_BF16, &nout[j]);
+        }
+        for (int64_t b = 0; b < nblk; ++b) {
+            double amax = 0.0;
+            for (int64_t j = b * KBLOCK; j < (b + 1) * KBLOCK; ++j) {
+                double y = fabs(bf16_value(nout[j]));
+                if (y > amax)
+                    amax = y;
+            }
+            /* FP32 quotients: an FP64 quotient of two FP32 values rounded to
+             * FP32 is the correctly rounded FP32 quotient */
+            float scale = (float)(amax / 448.0);
+            block_scale[i * nblk + b] = scale;
+            for (int64_t j = b * KBLOCK; j < (b + 1) * KBLOCK; ++j) {
+                double q = 0.0;
+                if (amax > 0.0)
+                    q = (double)(float)(bf16_value(nout[j]) / (double)scale);
+                oracle_e4m3_encode(&q, 1, &out[i * hidden + j]);
+            }
+        }
+    }
+    return 0;
+}

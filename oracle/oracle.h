@@ -6,8 +6,9 @@
  * baseline leg use it.  It shares no code, header, table or helper with the
  * CUDA library.
  *
- * What it computes is the plain definition of the operation on the MATE page
- * "FlashInfer Wrapper APIs", section GEMM:
+ * What it computes is the plain definition of the operations on the MATE page
+ * "FlashInfer Wrapper APIs", section GEMM (and, for the producer of the GEMM's
+ * FP8 activations, section Norm, declared further down):
  *   - gemm_fp8_nt_groupwise:            out = a @ b.T with FP32 scales at
  *                                       granularity (1, 128, 128)
  *   - group_deepgemm_fp8_nt_groupwise:  out[i] = a[i] @ b[m_indices[i]].T
@@ -112,6 +113,32 @@ int oracle_batch_gemm_masked_at(const uint8_t* a, const uint8_t* b,
                                 const int64_t* groups, const int64_t* rows,
                                 const int64_t* cols, int64_t count, double* ref,
                                 uint16_t* out, uint8_t* written);
+
+/* Encode values as E4M3 codes (float8_e4m3fn): round to nearest with ties to
+ * even on the format's grid (3 mantissa bits, subnormal quantum 2^-9) and
+ * saturate to +-448 (the format has no infinity); NaN gives 0x7F. */
+void oracle_e4m3_encode(const double* x, int64_t count, uint8_t* codes);
+
+/* fused_add_rmsnorm_fp8_block_quant of the MATE page "FlashInfer Wrapper
+ * APIs", section Norm: add `input` to `residual`, RMS-normalise the sum and
+ * quantise it to FP8 E4M3 with one FP32 scale per row-major 1 x 128 block.
+ * All BF16 tensors are passed as their 16-bit encodings; input, residual,
+ * residual_out and normed_out are (rows, hidden), weight is (hidden), out is
+ * (rows, hidden) E4M3 codes, block_scale is (rows, hidden / 128).  Per row:
+ *   x_j      = BF16(input_j + residual_j)                 -> residual_out
+ *   r        = 1 / sqrt(sum_j x_j^2 / hidden + eps)       (FP64)
+ *   y_j      = BF16(x_j * r * weight_j)                   -> normed_out
+ *   per block: amax = max |y_j|, scale = FP32(amax / 448) -> block_scale
+ *              code_j = E4M3(FP32(y_j / scale))           -> out
+ * (an all-zero block gets scale 0 and codes 0).  Returns -1 unless hidden is a
+ * positive multiple of 128 and rows >= 0. */
+int oracle_fused_add_rmsnorm_fp8_block_quant(const uint16_t* input,
+                                             const uint16_t* residual,
+                                             const uint16_t* weight, double eps,
+                                             int64_t rows, int64_t hidden,
+                                             uint16_t* residual_out,
+                                             uint16_t* normed_out, uint8_t* out,
+                                             float* block_scale);
 
 /* Number of threads the oracle's parallel loops use. */
 int oracle_num_threads(void);

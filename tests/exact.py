@@ -1,4 +1,5 @@
-"""Exact rational restatement of the groupwise FP8 GEMM, for tiny shapes.
+"""Exact rational restatements of the groupwise FP8 GEMM and of the fused
+add-RMSNorm + 1 x 128 FP8 quantisation, for tiny shapes.
 
 An independent second implementation used to pin the C oracle: E4M3 decoded
 from its bit fields into ``fractions.Fraction``, block sums in Python integers
@@ -16,6 +17,8 @@ FORMATS = {
     # largest finite value
     "bf16": (8, -126, Fraction(2 ** 8 - 1, 2 ** 7) * Fraction(2) ** 127),
     "f16": (11, -14, Fraction(65504)),
+    "f32": (24, -126, Fraction(2 ** 24 - 1, 2 ** 23) * Fraction(2) ** 127),
+    "e4m3": (4, -6, Fraction(448)),
 }
 
 
@@ -99,3 +102,73 @@ def dense(a_codes, b_codes, sa, sb, with_abs=False):
             R[i][j] = sum(terms, Fraction(0))
             A[i][j] = sum((abs(x) for x in terms), Fraction(0))
     return (R, A) if with_abs else R
+
+
+def bf16_value(bits):
+    """Exact value of a BF16 encoding (finite values only)."""
+    bits = int(bits)
+    s, e, f = bits >> 15, (bits >> 7) & 0xFF, bits & 0x7F
+    assert e != 0xFF
+    v = Fraction(f, 128) * Fraction(2) ** -126 if e == 0 else \
+        (1 + Fraction(f, 128)) * Fraction(2) ** (e - 127)
+    return -v if s else v
+
+
+def e4m3_code(v):
+    """E4M3 code of a value on the E4M3 grid with |v| <= 448."""
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            continue
+        if e4m3_value(c) == v and (v != 0 or c == 0):
+            return c
+    raise ValueError(v)
+
+
+def fused_add_rmsnorm_fp8_block_quant(input_bits, residual_bits, weight_bits, eps):
+    """fused_add_rmsnorm_fp8_block_quant (MATE page "FlashInfer Wrapper APIs",
+    section Norm) in exact arithmetic: the add and the sum of squares exactly,
+    the reciprocal square root to 80 significant digits (a BF16 rounding decision
+    is wrong only if the value lies within 1e-70 of a tie), every rounding by
+    exact comparison.  Returns (residual_bits, normed_bits, codes, scales) as
+    nested lists."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 80
+    rows, hidden = len(input_bits), len(input_bits[0])
+    w = [bf16_value(b) for b in weight_bits]
+    res_out, normed_out, codes, scales = [], [], [], []
+    for i in range(rows):
+        x = [round_exact(bf16_value(a) + bf16_value(b), "bf16")
+             for a, b in zip(input_bits[i], residual_bits[i])]
+        ms = sum(v * v for v in x) / hidden + Fraction(eps)
+        r = 1 / Decimal(ms.numerator).__truediv__(Decimal(ms.denominator)).sqrt()
+        y = [round_exact(Fraction(Decimal(v.numerator) / Decimal(v.denominator) * r
+                                  * Decimal(wj.numerator) / Decimal(wj.denominator)), "bf16")
+             for v, wj in zip(x, w)]
+        res_out.append([bf16_bits(v) for v in x])
+        normed_out.append([bf16_bits(v) for v in y])
+        crow, srow = [], []
+        for b0 in range(0, hidden, 128):
+            blk = y[b0:b0 + 128]
+            amax = max(abs(v) for v in blk)
+            scale = round_exact(amax / 448, "f32")
+            srow.append(float(scale))
+            for v in blk:
+                if amax == 0:
+                    crow.append(0)
+                    continue
+                q = round_exact(v / scale, "f32")
+                e = round_exact(q, "e4m3")
+                if isinstance(e, float) or abs(e) > 448:  # saturate
+                    e = Fraction(448) if q > 0 else Fraction(-448)
+                c = e4m3_code(e) if e != 0 else (0x80 if v < 0 else 0)
+                crow.append(c)
+        codes.append(crow)
+        scales.append(srow)
+    return res_out, normed_out, codes, scales
+
+
+def bf16_bits(v):
+    """BF16 encoding of a value on the BF16 grid."""
+    import struct
+    f = struct.pack(">f", float(v))
+    return int.from_bytes(f[:2], "big")
