@@ -34,6 +34,8 @@ if ROOT not in sys.path:
 
 METRIC = "FP8 groupwise GEMM TFLOP/s (device-timed) and % of GB300 dense FP8 roofline"
 UNIT = "TFLOP/s"
+NORM_METRIC = ("fused add-RMSNorm + 1x128 FP8 quantisation GB/s (device-timed) and % of GB300 "
+               "HBM roofline")
 DEFAULT_WORKLOAD = "dense_4096x7168x2048"
 L2_BYTES = 129 * 1024 * 1024
 FP8_OVER_BF16_NOMINAL = 4.5 / 2.25  # nominal dense FP8 / BF16 tensor rate
@@ -164,18 +166,33 @@ def max_over_ranks(x, device=None):
     return float(t.item())
 
 
-def throughput_tflops(world, flops_per_step, steps, slowest_ms):
-    """Whole-job TFLOP/s: the work of every rank over the slowest rank's time."""
-    return world * flops_per_step * steps / (slowest_ms * 1e-3) / 1e12
+def throughput_tflops(world, flops_per_step, steps, slowest_ms, divisor=1e12):
+    """Whole-job TFLOP/s (GB/s with divisor 1e9 and work in bytes): the work of
+    every rank over the slowest rank's time."""
+    return world * flops_per_step * steps / (slowest_ms * 1e-3) / divisor
 
 
 # --------------------------------------------------------------- workloads
+
+def metric_of(kind):
+    """(metric, unit, divisor) of a workload kind: GEMMs count FLOPs, the
+    HBM-bound norm + quantisation counts bytes."""
+    if kind == "norm":
+        return NORM_METRIC, "GB/s", 1e9
+    return METRIC, UNIT, 1e12
+
 
 def workload_stats(name, w):
     """Algorithmic FLOPs and bytes of one call (valid rows only)."""
     import workloads
     cfg = workloads.CONFIGS[name]
     kind = cfg["kind"]
+    if kind == "norm":
+        rows, hidden = w["rows"], w["hidden"]
+        # read input, residual; write residual, normed_out (BF16) and the codes
+        # (1 byte), plus the weight row and one FP32 scale per 128 elements
+        bytes_ = rows * hidden * (2 + 2 + 2 + 2 + 1) + 2 * hidden + 4 * rows * (hidden // 128)
+        return 0.0, bytes_, "hbm"
     k = w["k"]
     n = w["n"]
     kb, nb = k // 128, n // 128
@@ -228,6 +245,14 @@ def make_sets(name, device):
             elif cfg["kind"] == "grouped":
                 w = workloads.make(name, device=device, seed=seed)
                 w["out"] = torch.empty((w["m"], w["n"]), dtype=torch.bfloat16, device=device)
+            elif cfg["kind"] == "norm":
+                w = workloads.make(name, device=device, seed=seed)
+                rows, hidden = w["rows"], w["hidden"]
+                w["out"] = torch.empty((rows, hidden), dtype=torch.uint8, device=device)
+                w["block_scale"] = torch.empty((rows, hidden // 128), dtype=torch.float32,
+                                               device=device)
+                w["normed_out"] = torch.empty((rows, hidden), dtype=torch.bfloat16,
+                                              device=device)
             else:
                 w = workloads.make(name, device=device, seed=seed)
                 w["out"] = torch.empty((w["num_groups"], w["max_m"], w["n"]),
@@ -253,6 +278,11 @@ def call_args(lib, name, w, stream_handle):
         return (lib.fp8_gemm_nt_groupwise,
                 (p(w["a"]), p(w["b"]), p(w["a_scale"]), p(w["b_scale"]), p(w["out"]), od,
                  w["m"], w["n"], w["k"], sm, 1, 128, 128, 0, stream_handle))
+    if kind == "norm":
+        return (lib.fused_add_rmsnorm_fp8_block_quant,
+                (p(w["out"]), p(w["block_scale"]), p(w["normed_out"]), p(w["input"]),
+                 p(w["residual"]), p(w["weight"]), w["eps"], w["rows"], w["hidden"],
+                 stream_handle))
     if kind == "grouped":
         return (lib.fp8_group_gemm_contiguous,
                 (p(w["a"]), p(w["b"]), p(w["a_scale"]), p(w["b_scale"]), p(w["m_indices"]),
@@ -266,8 +296,10 @@ def call_args(lib, name, w, stream_handle):
 # ------------------------------------------------------------ oracle timing
 
 def oracle_sample_rate(name, w, seconds, seed=21):
-    """Time the oracle on a bounded sample of output elements of one call.
-    Returns (flops_per_second, samples, seconds_taken, threads, positions, ref)."""
+    """Time the oracle on a bounded sample of one call: output elements of a
+    GEMM, rows of the norm + quantisation.  Returns (work_per_second, samples,
+    seconds_taken, threads, positions, ref, written), work in FLOPs (GEMMs) or
+    algorithmic bytes (norm)."""
     import numpy as np
     import oracle
     import workloads
@@ -276,6 +308,12 @@ def oracle_sample_rate(name, w, seconds, seed=21):
 
     def run(count):
         g = np.random.default_rng(seed)
+        if cfg["kind"] == "norm":
+            r = np.sort(g.choice(host["rows"], size=min(count, host["rows"]), replace=False))
+            t0 = time.perf_counter()
+            ref = oracle.fused_add_rmsnorm_fp8_block_quant(host["input"][r], host["residual"][r],
+                                                           host["weight"], host["eps"])
+            return time.perf_counter() - t0, r, ref, np.ones(r.size, bool)
         if cfg["kind"] == "dense":
             r = g.integers(0, host["m"], count)
             c = g.integers(0, host["n"], count)
@@ -307,16 +345,23 @@ def oracle_sample_rate(name, w, seconds, seed=21):
 
     # grow a probe until it takes a measurable time, then size the sample to
     # about `seconds` of oracle work
-    count = 4096
+    if cfg["kind"] == "norm":
+        count, limit = 4, host["rows"]
+    else:
+        count, limit = 4096, 50_000_000
     while True:
         dt, _, _, _ = run(count)
-        if dt >= min(0.5, seconds / 4) or count >= 50_000_000:
+        if dt >= min(0.5, seconds / 4) or count >= limit:
             break
         count *= 4
-    count = int(max(count, min(50_000_000, count * seconds / max(dt, 1e-6))))
+    count = int(max(1, min(limit, max(count, count * seconds / max(dt, 1e-6)))))
     dt, pos, ref, wr = run(count)
-    flops = 2.0 * host["k"] * int(wr.sum())
-    return flops / dt, count, dt, oracle.num_threads(), pos, ref, wr
+    if cfg["kind"] == "norm":
+        _, row_bytes, _ = workload_stats(name, dict(rows=1, hidden=host["hidden"]))
+        work = row_bytes * int(wr.sum())  # algorithmic bytes of the sampled rows
+    else:
+        work = 2.0 * host["k"] * int(wr.sum())
+    return work / dt, count, dt, oracle.num_threads(), pos, ref, wr
 
 
 # ------------------------------------------------------------------ arms
@@ -327,6 +372,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import workloads
+    metric, unit, div = metric_of(workloads.CONFIGS[args.workload]["kind"])
     w = workloads.make(args.workload, device="cpu")
     total = args.steps + args.warmup
     per_step = max(0.05, min(5.0, args.cpu_seconds / 2, 150.0 / max(total, 1)))
@@ -340,18 +386,20 @@ def run_reference(args):
             times.append(d)
             flops += r * d
     elapsed = sum(times)
-    value = flops / elapsed / 1e12
+    value = flops / elapsed / div
+    what = ("seeded rows per step of %s (add, RMSNorm and 1x128 quantisation of each row in "
+            "FP64)" if workloads.CONFIGS[args.workload]["kind"] == "norm" else
+            "seeded output elements per step of %s (each the full k-long FP64 dot product and "
+            "scale promotion)")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "impl": "reference", "metric": metric, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * elapsed / max(args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": "%d seeded output elements per step of %s (each the full "
-                                   "k-long FP64 dot product and scale promotion)"
-                                   % (count, args.workload)},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+                         "sample": "%d " % count + what % args.workload},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -375,9 +423,13 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
+    kind = workload_kind(args.workload)
+    metric, unit_v, div = metric_of(kind)
     sets, calls_per_step = make_sets(args.workload, dev)
     flops_call, bytes_call, bound = workload_stats(args.workload, sets[0][0])
-    flops_step = flops_call * calls_per_step
+    # the unit of `value`: FLOPs for the GEMMs, algorithmic bytes for the norm
+    work_call = bytes_call if kind == "norm" else flops_call
+    flops_step = work_call * calls_per_step
     calls = [[call_args(lib, args.workload, w, sh) for w in one] for one in sets]
 
     def step(i):
@@ -430,22 +482,25 @@ def run_ours(args):
         for w in one:
             hs.append({k: v.cpu().pin_memory() for k, v in w.items() if torch.is_tensor(v)})
         host_sets.append(hs)
-    h2d = sum(v.numel() * v.element_size() for hs in host_sets[0] for k, v in hs.items()
-              if k != "out")
-    d2h = sum(hs["out"].numel() * hs["out"].element_size() for hs in host_sets[0])
+    out_keys = OUTPUT_KEYS.get(kind, ("out",))
+    in_keys = INPUT_KEYS.get(kind)
+    if in_keys is None:
+        in_keys = tuple(k for k in host_sets[0][0] if k != "out")
+    h2d = sum(hs[k].numel() * hs[k].element_size() for hs in host_sets[0] for k in in_keys)
+    d2h = sum(hs[k].numel() * hs[k].element_size() for hs in host_sets[0] for k in out_keys)
     e2e_steps = max(3, min(args.steps, 50))
 
     def e2e_step():
         for w, hs in zip(sets[0], host_sets[0]):
-            for k, v in hs.items():
-                if k != "out":
-                    w[k].copy_(v, non_blocking=True)
+            for k in in_keys:
+                w[k].copy_(hs[k], non_blocking=True)
         for fn, a in calls[0]:
             rc = fn(*a)
             if rc != 0:
                 raise fp8g.Fp8gError(rc, fn.__name__, fp8g.last_error())
         for w, hs in zip(sets[0], host_sets[0]):
-            hs["out"].copy_(w["out"], non_blocking=True)
+            for k in out_keys:
+                hs[k].copy_(w[k], non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -458,13 +513,14 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
-    e2e_value = throughput_tflops(world, flops_step, e2e_steps, max_over_ranks(e2e_ms, dev))
-    value = throughput_tflops(world, flops_step, args.steps, region_ms)
+    e2e_value = throughput_tflops(world, flops_step, e2e_steps, max_over_ranks(e2e_ms, dev), div)
+    value = throughput_tflops(world, flops_step, args.steps, region_ms, div)
     launches = args.steps * calls_per_step
     avg_launch_s = region_ms * 1e-3 / launches
     peaks, peaks_src = load_peaks()
     kernel_name = {"dense": "gemm_kernel<dense>", "grouped": "gemm_kernel<grouped>",
-                   "masked": "gemm_kernel<masked>"}[workload_kind(args.workload)]
+                   "masked": "gemm_kernel<masked>",
+                   "norm": "fused_add_rmsnorm_quant_kernel"}[kind]
     if bound == "tensor":
         achieved = flops_call / avg_launch_s / 1e12
         peak = fp8_peak_tflops(peaks)
@@ -485,30 +541,39 @@ def run_ours(args):
     spot = None
     if rank == 0 and not args.no_cpu_baseline:
         w0 = sets[0][0]
-        rate, count, dt, threads, pos, ref, wr = oracle_sample_rate(args.workload, w0,
+        # the inputs of set 0's last call: the end-to-end loop copied them from
+        # these host buffers (the norm updates `residual` in place)
+        src = dict(w0)
+        src.update({k: host_sets[0][0][k] for k in in_keys})
+        rate, count, dt, threads, pos, ref, wr = oracle_sample_rate(args.workload, src,
                                                                     args.cpu_seconds)
-        cpu_baseline = {"value": rate / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-                        "sample": "%d seeded output elements of one %s call (%.1f s)"
-                                  % (count, args.workload, dt)}
+        cpu_baseline = {"value": rate / div, "unit": unit_v, "cores": threads, "kind": "oracle",
+                        "sample": "%d seeded %s of one %s call (%.1f s)"
+                                  % (count, "rows" if kind == "norm" else "output elements",
+                                     args.workload, dt)}
         # spot check of the benchmarked kernel's output at the oracle's positions
         # (set 0 was last written by the end-to-end loop from the same inputs)
         torch.cuda.synchronize(dev)
-        got = w0["out"].float().cpu().double().numpy()[tuple(pos)]
-        ref = np.asarray(ref)
-        rms = float(np.sqrt(np.mean(ref[wr] ** 2)))
-        ok = bool(np.all(np.abs(got[wr] - ref[wr]) <= 1e-2 * np.abs(ref[wr]) + 2e-3 * rms))
-        spot = {"elements": int(wr.sum()), "within_tolerance": ok}
+        if kind == "norm":
+            spot = norm_spot_check(w0, pos, ref)
+        else:
+            got = w0["out"].float().cpu().double().numpy()[tuple(pos)]
+            ref = np.asarray(ref)
+            rms = float(np.sqrt(np.mean(ref[wr] ** 2)))
+            ok = bool(np.all(np.abs(got[wr] - ref[wr]) <= 1e-2 * np.abs(ref[wr]) + 2e-3 * rms))
+            spot = {"elements": int(wr.sum()), "within_tolerance": ok}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "metric": metric, "value": value, "unit": unit_v, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": region_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if kind == "norm" else "fp8_e4m3",
             "data": "synthetic",
             "config": config_block(args.workload, sets, calls_per_step, world),
             "roofline": roofline, "cpu_baseline": cpu_baseline,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "e2e": {"value": e2e_value, "unit": unit_v, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": launches, "clocks": clocks, "spot_check": spot,
             "device_status": status,
@@ -517,6 +582,35 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+# tensors copied in and out by the end-to-end leg (default: everything but
+# `out` in, `out` back)
+INPUT_KEYS = {"norm": ("input", "residual", "weight")}
+OUTPUT_KEYS = {"norm": ("out", "block_scale", "normed_out", "residual")}
+
+
+def norm_spot_check(w, rows, ref):
+    """The norm + quantisation's output on the oracle's rows: the residual sum
+    bit-exact, normed_out within one BF16 unit, codes and scales bit-exact in
+    every block whose normed_out equals the oracle's."""
+    import numpy as np
+    import torch
+    idx = torch.as_tensor(rows, device=w["out"].device)
+    got_res = w["residual"][idx].cpu().view(torch.int16).numpy().view(np.uint16)
+    got_n = w["normed_out"][idx].cpu().view(torch.int16).numpy().view(np.uint16)
+    got_c = w["out"][idx].cpu().numpy()
+    got_s = w["block_scale"][idx].cpu().numpy()
+    f = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)  # noqa: E731
+    ok = bool(np.array_equal(got_res, ref["residual_out"]))
+    gn, rn = f(got_n), f(ref["normed_out"])
+    ok &= bool(np.all(np.abs(gn - rn) <= np.abs(rn) * 2.0 ** -7 + 1e-38))
+    same = (got_n == ref["normed_out"]).reshape(len(rows), -1, 128).all(axis=2)
+    gc = got_c.reshape(len(rows), -1, 128)
+    rc = ref["out"].reshape(len(rows), -1, 128)
+    ok &= bool(np.array_equal(gc[same], rc[same]))
+    ok &= bool(np.array_equal(got_s[same], ref["block_scale"][same]))
+    return {"elements": int(got_n.size), "rows": int(len(rows)), "within_tolerance": ok}
 
 
 def workload_kind(name):

@@ -5,8 +5,8 @@ arguments — tensor pointers, sizes, the current CUDA stream — and raises on 
 non-zero status; every step of the computation runs in the library's CUDA
 kernels.  If ``libfp8g.so`` is missing, calls fail: there is no other path.
 
-Two layers, both following the MATE page "FlashInfer Wrapper APIs", section
-GEMM:
+Two layers of GEMM calls, both following the MATE page "FlashInfer Wrapper
+APIs", section GEMM:
 
 * ``fp8_gemm_nt_groupwise``, ``fp8_group_gemm_contiguous``,
   ``fp8_batch_gemm_masked`` — the C entry points, same names, taking tensors
@@ -14,6 +14,10 @@ GEMM:
 * ``gemm_fp8_nt_groupwise``, ``group_deepgemm_fp8_nt_groupwise``,
   ``batch_deepgemm_fp8_nt_groupwise`` — the page's own signatures, which
   allocate ``out`` when it is omitted and return it.
+
+and ``fused_add_rmsnorm_fp8_block_quant`` (section Norm, same name and argument
+order as the page), which produces the GEMMs' FP8 activations and K-major
+1 x 128 scales.
 
 E4M3 operands may be ``torch.float8_e4m3fn`` or ``torch.uint8`` (raw codes).
 """
@@ -24,7 +28,7 @@ __all__ = [
     "Fp8gError", "load", "last_error", "get_device_status",
     "fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
     "gemm_fp8_nt_groupwise", "group_deepgemm_fp8_nt_groupwise",
-    "batch_deepgemm_fp8_nt_groupwise",
+    "batch_deepgemm_fp8_nt_groupwise", "fused_add_rmsnorm_fp8_block_quant",
     "OK", "ERR_INVALID_ARGUMENT", "ERR_UNSUPPORTED", "ERR_ARCH", "ERR_CUDA", "ERR_TIMEOUT",
     "DEVICE_TIMEOUT", "DEVICE_BAD_M_INDICES", "DEVICE_MASKED_M_CLAMPED",
 ]
@@ -62,8 +66,10 @@ def load():
     lib.fp8_group_gemm_contiguous.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, P]
     lib.fp8_batch_gemm_masked.argtypes = [P, P, P, P, P, I64, P, I64, I64, I64, I64, P]
     lib.fp8g_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
+    lib.fused_add_rmsnorm_fp8_block_quant.argtypes = [P, P, P, P, P, P, ctypes.c_float, I64,
+                                                      I64, P]
     for f in ("fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
-              "fp8g_get_device_status"):
+              "fused_add_rmsnorm_fp8_block_quant", "fp8g_get_device_status"):
         getattr(lib, f).restype = ctypes.c_int
     lib.fp8g_last_error.argtypes = []
     lib.fp8g_last_error.restype = ctypes.c_char_p
@@ -225,6 +231,35 @@ def fp8_batch_gemm_masked(a, b, a_scale, b_scale, masked_m, expected_m, out, str
         _ptr(out), g, max_m, n, k, _stream_handle(stream, dev))
     _raise_on(rc, "fp8_batch_gemm_masked")
     return out
+
+
+def fused_add_rmsnorm_fp8_block_quant(out, block_scale, normed_out, input, residual, weight,
+                                      eps=1e-6, enable_pdl=None, stream=None):
+    """residual += input; normed_out = RMSNorm(residual) * weight; out, block_scale =
+    row-major 1 x 128 E4M3 quantisation of normed_out (scales are multipliers).
+
+    ``enable_pdl`` is accepted for the page's signature: every launch of this
+    library already lets its prologue overlap the previous kernel.
+    """
+    torch = _torch()
+    del enable_pdl
+    _e4m3(out, "out")
+    _need(input.dim() == 2, "input must be (rows, hidden)")
+    rows, hidden = input.shape
+    for t, nm in ((input, "input"), (residual, "residual"), (normed_out, "normed_out")):
+        _need(t.dtype == torch.bfloat16 and tuple(t.shape) == (rows, hidden),
+              "%s must be bfloat16 (%d, %d)" % (nm, rows, hidden))
+    _need(weight.dtype == torch.bfloat16 and tuple(weight.shape) == (hidden,),
+          "weight must be bfloat16 (%d,)" % hidden)
+    _need(tuple(out.shape) == (rows, hidden), "out must be (%d, %d)" % (rows, hidden))
+    _need(block_scale.dtype == torch.float32 and tuple(block_scale.shape) == (rows, hidden // 128),
+          "block_scale must be float32 (rows, hidden // 128)")
+    dev = _cuda_contig((out, block_scale, normed_out, input, residual, weight),
+                       ("out", "block_scale", "normed_out", "input", "residual", "weight"))
+    rc = load().fused_add_rmsnorm_fp8_block_quant(
+        _ptr(out), _ptr(block_scale), _ptr(normed_out), _ptr(input), _ptr(residual),
+        _ptr(weight), float(eps), rows, hidden, _stream_handle(stream, dev))
+    _raise_on(rc, "fused_add_rmsnorm_fp8_block_quant")
 
 
 # ------------------------------------------------------------- page signatures

@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -18,6 +19,7 @@
 
 #include "fp8g.h"
 #include "gemm_kernel.cuh"
+#include "norm_quant.cuh"
 
 namespace {
 
@@ -52,6 +54,7 @@ struct DeviceState {
     int sm_count = 0;
     unsigned int* status = nullptr;
     bool kernel_ready[kNumKernels] = {};
+    bool norm_ready = false;
     int resident[kNumKernels] = {};  // CTAs (or CTA pairs) of a persistent grid
 };
 
@@ -376,6 +379,70 @@ fp8g_status_t fp8_batch_gemm_masked(const void* a, const void* b, const float* a
         p.masked_m = masked_m;
         p.status = ds->status;
         return launch<fp8g::FORM_MASKED, __nv_bfloat16, false>(*ds, 3, map_a, map_b, p, tiles, stream);
+    } catch (...) {
+        return fail(FP8G_ERR_CUDA, "unexpected exception");
+    }
+}
+
+fp8g_status_t fused_add_rmsnorm_fp8_block_quant(void* out, float* block_scale, void* normed_out,
+                                                const void* input, void* residual,
+                                                const void* weight, float eps, int64_t rows,
+                                                int64_t hidden, cudaStream_t stream) {
+    try {
+        if (rows < 0) return fail(FP8G_ERR_INVALID_ARGUMENT, "rows = %lld < 0", (long long)rows);
+        if (hidden <= 0 || hidden % 128)
+            return fail(FP8G_ERR_INVALID_ARGUMENT,
+                        "hidden = %lld must be a positive multiple of 128", (long long)hidden);
+        if (hidden > 65536)
+            return fail(FP8G_ERR_UNSUPPORTED, "hidden = %lld > 65536", (long long)hidden);
+        if (!(eps >= 0.0f) || !std::isfinite(eps))
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "eps must be finite and >= 0");
+        if (rows > kMaxDim) return fail(FP8G_ERR_UNSUPPORTED, "rows must be < 2^31");
+        if (rows == 0) {
+            t_last_error.clear();
+            return FP8G_OK;
+        }
+        if (!out || !block_scale || !normed_out || !input || !residual || !weight)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "null pointer argument");
+        if (!aligned(out, 16) || !aligned(normed_out, 16) || !aligned(input, 16) ||
+            !aligned(residual, 16) || !aligned(weight, 16) || !aligned(block_scale, 4))
+            return fail(FP8G_ERR_INVALID_ARGUMENT,
+                        "out, normed_out, input, residual and weight must be 16-byte aligned, "
+                        "block_scale 4-byte aligned");
+        DeviceState* ds = nullptr;
+        fp8g_status_t s = device_state(&ds);
+        if (s != FP8G_OK) return s;
+        const size_t smem = static_cast<size_t>(hidden) * 2;
+        auto kernel = fp8g::fused_add_rmsnorm_quant_kernel;
+        {
+            std::lock_guard<std::mutex> lock(g_mutex);
+            if (!ds->norm_ready) {
+                cudaError_t e = cudaFuncSetAttribute(
+                    kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536 * 2);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+                ds->norm_ready = true;
+            }
+        }
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(rows), 1, 1);
+        cfg.blockDim = dim3(fp8g::NQ_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        (void)cudaGetLastError();
+        cudaError_t e = cudaLaunchKernelEx(
+            &cfg, kernel, static_cast<uint8_t*>(out), block_scale, static_cast<uint16_t*>(normed_out),
+            static_cast<const uint16_t*>(input), static_cast<uint16_t*>(residual),
+            static_cast<const uint16_t*>(weight), eps, static_cast<int>(rows),
+            static_cast<int>(hidden));
+        if (e == cudaSuccess) e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+        t_last_error.clear();
+        return FP8G_OK;
     } catch (...) {
         return fail(FP8G_ERR_CUDA, "unexpected exception");
     }

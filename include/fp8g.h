@@ -1,8 +1,9 @@
 /*
  * fp8g — FP8 (E4M3) groupwise-scaled NT GEMM for sm_103a (GB300).
  *
- * C ABI of the library.  Three operations, as defined on the MATE page
- * "FlashInfer Wrapper APIs", section GEMM:
+ * C ABI of the library.  Three GEMMs, as defined on the MATE page
+ * "FlashInfer Wrapper APIs", section GEMM, and the kernel that produces their
+ * FP8 activations (section Norm, fused_add_rmsnorm_fp8_block_quant, below):
  *
  *   fp8_gemm_nt_groupwise       gemm_fp8_nt_groupwise            out = a @ b.T
  *   fp8_group_gemm_contiguous   group_deepgemm_fp8_nt_groupwise  out[i] = a[i] @ b[m_indices[i]].T
@@ -136,6 +137,41 @@ fp8g_status_t fp8_batch_gemm_masked(const void* a, const void* b,
                                     const int32_t* masked_m, int64_t expected_m,
                                     void* out, int64_t num_groups, int64_t max_m,
                                     int64_t n, int64_t k, cudaStream_t stream);
+
+/*
+ * Fused add + RMSNorm + row-major 1 x 128 FP8 quantisation, the producer of the
+ * GEMMs' `a` and K-major `a_scale` (page: fused_add_rmsnorm_fp8_block_quant,
+ * section Norm).  Per row of `hidden` BF16 values:
+ *
+ *   residual_j   <- BF16(input_j + residual_j)                 (in place)
+ *   normed_out_j  = BF16(residual_j * r * weight_j),  r = 1 / sqrt(mean(residual^2) + eps)
+ *   for every 128-column block b:
+ *     block_scale[b] = amax_b / 448 (FP32), amax_b = max over the block of |normed_out_j|
+ *     out_j          = E4M3(normed_out_j / block_scale[b]), round to nearest even,
+ *                      saturated to +-448; an all-zero block gets scale 0, codes 0
+ *
+ * so that normed_out_j ~= out_j * block_scale[b] (the scales are multipliers,
+ * as the GEMMs' a_scale).
+ *
+ *   out          (rows, hidden) E4M3 codes.
+ *   block_scale  FP32 (rows, hidden/128), row-major (the GEMMs' K-major a_scale).
+ *   normed_out   (rows, hidden) BF16.
+ *   input        (rows, hidden) BF16, read only.
+ *   residual     (rows, hidden) BF16, read and overwritten with input + residual.
+ *   weight       (hidden) BF16.
+ *   eps          added to the mean square (page default 1e-6), >= 0.
+ *   hidden must be a positive multiple of 128 and at most 65536; rows >= 0
+ *   (0 launches nothing).  out, normed_out, input, residual and weight 16-byte
+ *   aligned, block_scale 4-byte aligned; the arrays must not overlap.
+ *   Accumulation is FP32, so normed_out may differ from an exact computation
+ *   by one BF16 unit in the last place where the exact value is close to a
+ *   rounding boundary; the codes and scales are a deterministic function of
+ *   normed_out.
+ */
+fp8g_status_t fused_add_rmsnorm_fp8_block_quant(void* out, float* block_scale, void* normed_out,
+                                                const void* input, void* residual,
+                                                const void* weight, float eps, int64_t rows,
+                                                int64_t hidden, cudaStream_t stream);
 
 /* Message of the last failed call on this thread ("" if none); valid until the
  * thread's next call into the library. */

@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_three_forms_and_helpers():
     names = declared_functions()
     for f in ("fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
-              "fp8g_last_error", "fp8g_get_device_status"):
+              "fused_add_rmsnorm_fp8_block_quant", "fp8g_last_error", "fp8g_get_device_status"):
         assert f in names
 
 
@@ -104,6 +104,33 @@ def test_masked_host_validation(lib):
     assert h.fp8_batch_gemm_masked(16, 16, 16, 16, 0, 1, 16, 4, 256, 256, 256, None) == 1
     assert "masked_m" in lib.last_error()
     assert h.fp8_batch_gemm_masked(16, 16, 16, 16, 16, 1, 16, -1, 256, 256, 256, None) == 1
+
+
+def _norm(h, out=16, bs=16, normed=16, inp=16, res=16, w=16, eps=1e-6, rows=4, hidden=256):
+    return h.fused_add_rmsnorm_fp8_block_quant(out, bs, normed, inp, res, w, eps, rows, hidden,
+                                               None)
+
+
+@pytest.mark.parametrize("kwargs,status,msg", [
+    (dict(hidden=200), 1, "hidden = 200"),
+    (dict(hidden=0), 1, "hidden = 0"),
+    (dict(hidden=65536 + 128), 2, "65536"),
+    (dict(rows=-1), 1, "rows = -1"),
+    (dict(eps=float("nan")), 1, "eps"),
+    (dict(eps=-1.0), 1, "eps"),
+    (dict(out=0), 1, "null"),
+    (dict(w=0), 1, "null"),
+    (dict(res=24), 1, "16-byte"),
+    (dict(bs=18), 1, "4-byte"),
+])
+def test_norm_quant_host_validation(lib, kwargs, status, msg):
+    h = lib.load()
+    assert _norm(h, **kwargs) == status
+    assert msg in lib.last_error()
+
+
+def test_norm_quant_empty_is_ok_without_device(lib):
+    assert _norm(lib.load(), rows=0, out=0, inp=0) == 0
 
 
 def test_valid_call_without_a_device_reports_cuda_error(lib):

@@ -83,3 +83,27 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference"],
                        capture_output=True, text=True, timeout=300, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_norm_workload_counts_bytes_against_hbm():
+    sys.path.insert(0, ROOT)
+    import bench
+    metric, unit, div = bench.metric_of("norm")
+    assert unit == "GB/s" and div == 1e9 and "GB/s" in metric
+    flops, nbytes, bound = bench.workload_stats("norm_quant_4096x7168",
+                                                dict(rows=4096, hidden=7168))
+    assert flops == 0.0 and bound == "hbm"
+    # 4 bytes read and 5 written per element, the weight row, one scale per 128
+    assert nbytes == 4096 * 7168 * 9 + 2 * 7168 + 4 * 4096 * 56
+    assert bench.throughput_tflops(1, 1e9, 5, 1000.0, 1e9) == pytest.approx(5.0)
+
+
+def test_reference_arm_norm_workload_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "norm_quant_4096x7168", "--steps", "2", "--warmup", "1",
+                        "--cpu-seconds", "0.5"], capture_output=True, text=True, cwd=ROOT,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and "rows" in line["cpu_baseline"]["sample"]

@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the FP8 groupwise-scaled NT GEMM.
+"""Seeded synthetic inputs for the FP8 groupwise-scaled NT GEMM and for the
+fused add-RMSNorm + 1 x 128 FP8 quantisation that produces its activations.
 
 This module only draws random numbers and packs them into the operand layouts
 of the MATE page "FlashInfer Wrapper APIs", section GEMM; it holds none of the
@@ -36,6 +37,9 @@ CONFIGS = {
         scale_exp=(-6.0, 0.0), seed=1004),
     "dense_16384x18432x7168": dict(kind="dense", m=16384, n=18432, k=7168, dist="normal",
                                    scale_exp=(-6.0, 0.0), out_dtype="f16", seed=1005),
+    # the producer of the GEMM's activations: 4096 tokens of hidden size 7168
+    # (the k of the MoE workloads above)
+    "norm_quant_4096x7168": dict(kind="norm", rows=4096, hidden=7168, eps=1e-6, seed=1006),
 }
 
 
@@ -153,6 +157,21 @@ def masked(num_groups, max_m, n, k, seed, scale_exp=(-6.0, 0.0), expected_m=None
                 expected_m=expected_m if expected_m is not None else max_m // 2)
 
 
+def norm(rows, hidden, seed, eps=1e-6, device="cpu", **_):
+    """Operands of fused_add_rmsnorm_fp8_block_quant: BF16 input and residual
+    ~ N(0, 1), BF16 weight ~ 1 + N(0, 0.2^2) (RMSNorm gains near one)."""
+    gen = generator(seed, device)
+    x = torch.empty((rows, hidden), dtype=torch.float32, device=device)
+    x.normal_(0.0, 1.0, generator=gen)
+    inp = x.to(torch.bfloat16)
+    x.normal_(0.0, 1.0, generator=gen)
+    res = x.to(torch.bfloat16)
+    w = torch.empty((hidden,), dtype=torch.float32, device=device)
+    w.normal_(0.0, 0.2, generator=gen)
+    return dict(input=inp, residual=res, weight=(w + 1.0).to(torch.bfloat16), rows=rows,
+                hidden=hidden, eps=eps)
+
+
 def make(name, device="cpu", **overrides):
     """Operands of one of the named workloads."""
     cfg = dict(CONFIGS[name])
@@ -164,6 +183,8 @@ def make(name, device="cpu", **overrides):
         return grouped(device=device, **cfg)
     if kind == "masked":
         return masked(device=device, **cfg)
+    if kind == "norm":
+        return norm(device=device, **cfg)
     raise ValueError(kind)
 
 
