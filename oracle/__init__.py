@@ -251,3 +251,13 @@ def fused_add_rmsnorm_fp8_block_quant(input_bits, residual_bits, weight_bits, ep
         _p(res["normed_out"]), _p(res["out"]), _p(res["block_scale"]))
     _check(rc, "fused_add_rmsnorm_fp8_block_quant")
     return res
+
+
+def quantize_output_e4m3(ref, output_scale):
+    """FP8 output of gemm_fp8_nt_groupwise with output_scale (MATE page
+    "FlashInfer Wrapper APIs", section GEMM): E4M3 codes of R / s, R the exact
+    (FP64) result and s the FP32 output scale, rounded to nearest even and
+    saturated to +-448 — the scale multiplies codes back into values, as a_scale
+    and b_scale do."""
+    r = np.asarray(ref, np.float64)
+    return e4m3_encode(r / float(np.float32(output_scale)))

@@ -344,3 +344,45 @@ def test_masked_sampled_equals_full(oracle_mod):
         w["a"], w["b"], w["a_scale"], w["b_scale"], w["masked_m"], gs, rs_, cs)
     assert np.array_equal(wr, written[gs, rs_, cs])
     assert np.array_equal(r[wr], ref[gs, rs_, cs][wr]) and np.array_equal(b[wr], bits[gs, rs_, cs][wr])
+
+
+def test_fp8_output_hand_worked_codes(oracle_mod):
+    # FP8 output with output_scale (section GEMM): a = b = 1 (code 0x38),
+    # k = 256, unit scales, so every R = 256 exactly; code = E4M3(256 / s).
+    m, n, k = 2, 128, 256
+    a = np.full((m, k), 0x38, np.uint8)
+    b = np.full((n, k), 0x38, np.uint8)
+    ref, _ = oracle_mod.gemm_nt_groupwise(a, b, np.ones((m, 2), np.float32),
+                                          np.ones((1, 2), np.float32))
+    assert np.all(ref == 256.0)
+    # s = 1: 256 = 1.0 x 2^8 -> exponent field 15, mantissa 0 -> 0x78
+    # s = 4: 64 = 2^6 -> exponent field 13 -> 0x68
+    # s = 3: 85.33 lies in [64, 128) where the E4M3 quantum is 8: 10.67 quanta -> 88
+    #        = 1.375 x 2^6 -> exponent field 13, mantissa 3 -> 0x6B
+    # s = 0.5: 512 is past 448 -> saturates to 0x7E
+    # s = -2: -128 = -(2^7) -> sign, exponent field 14 -> 0xF0
+    for s, code in ((1.0, 0x78), (4.0, 0x68), (3.0, 0x6B), (0.5, 0x7E), (-2.0, 0xF0)):
+        assert np.all(oracle_mod.quantize_output_e4m3(ref, s) == code), s
+
+
+def test_fp8_output_is_the_encoder_of_the_scaled_result(oracle_mod):
+    # Against torch: float32 results divided by a power-of-two scale (exact),
+    # cast with float8_e4m3fn after clamping to the finite range.
+    import torch
+    g = np.random.default_rng(4)
+    m, n, k = 64, 256, 384
+    # values with at most two significant bits keep every result exact in FP32
+    vals = np.array([0.0, 0.5, -0.5, 1.0, -1.0, 1.5, -1.5, 2.0, -2.0, 3.0, -3.0], np.float32)
+    a = torch.from_numpy(vals[g.integers(0, vals.size, (m, k))]) \
+        .to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    b = torch.from_numpy(vals[g.integers(0, vals.size, (n, k))]) \
+        .to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    sa = np.exp2(g.integers(-3, 2, (m, 3))).astype(np.float32)
+    sb = np.exp2(g.integers(-3, 2, (2, 3))).astype(np.float32)
+    ref, _ = oracle_mod.gemm_nt_groupwise(a, b, sa, sb)
+    # the products of codes and power-of-two scales are exact in FP32 here
+    assert np.array_equal(ref.astype(np.float32).astype(np.float64), ref)
+    for s in (0.125, 1.0, 8.0):
+        want = torch.from_numpy((ref / s).astype(np.float32)).clamp(-448, 448) \
+            .to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(oracle_mod.quantize_output_e4m3(ref, s), want)
