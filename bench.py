@@ -198,7 +198,7 @@ def workload_stats(name, w):
     kb, nb = k // 128, n // 128
     if kind == "dense":
         m = w["m"]
-        out_b = 2
+        out_b = 1 if "output_scale" in w else 2
         flops = 2.0 * m * n * k
         bytes_ = m * k + n * k + 4 * (m * kb + nb * kb) + out_b * m * n
         return flops, bytes_, "tensor"
@@ -240,7 +240,8 @@ def make_sets(name, device):
             seed = cfg["seed"] + 100 * s + li
             if cfg["kind"] == "dense":
                 w = workloads.make(name, device=device, seed=seed, scale_major=major)
-                odt = torch.float16 if cfg["out_dtype"] == "f16" else torch.bfloat16
+                odt = {"f16": torch.float16, "e4m3": torch.uint8}.get(cfg["out_dtype"],
+                                                                      torch.bfloat16)
                 w["out"] = torch.empty((w["m"], w["n"]), dtype=odt, device=device)
             elif cfg["kind"] == "grouped":
                 w = workloads.make(name, device=device, seed=seed)
@@ -275,9 +276,13 @@ def call_args(lib, name, w, stream_handle):
         import torch
         od = 1 if w["out"].dtype == torch.float16 else 0
         sm = 1 if w["scale_major"] == "MN" else 0
+        os_ = w.get("output_scale")
+        if os_ is not None:
+            od = 2  # E4M3 codes with a per-tensor output scale
         return (lib.fp8_gemm_nt_groupwise,
                 (p(w["a"]), p(w["b"]), p(w["a_scale"]), p(w["b_scale"]), p(w["out"]), od,
-                 w["m"], w["n"], w["k"], sm, 1, 128, 128, 0, stream_handle))
+                 p(os_) if os_ is not None else None, w["m"], w["n"], w["k"], sm, 1, 128, 128, 0,
+                 stream_handle))
     if kind == "norm":
         return (lib.fused_add_rmsnorm_fp8_block_quant,
                 (p(w["out"]), p(w["block_scale"]), p(w["normed_out"]), p(w["input"]),
@@ -557,10 +562,20 @@ def run_ours(args):
         if kind == "norm":
             spot = norm_spot_check(w0, pos, ref)
         else:
-            got = w0["out"].float().cpu().double().numpy()[tuple(pos)]
             ref = np.asarray(ref)
             rms = float(np.sqrt(np.mean(ref[wr] ** 2)))
-            ok = bool(np.all(np.abs(got[wr] - ref[wr]) <= 1e-2 * np.abs(ref[wr]) + 2e-3 * rms))
+            tol = 1e-2 * np.abs(ref[wr]) + 2e-3 * rms
+            if "output_scale" in w0:
+                # E4M3 codes of R / s: within one E4M3 step of the exact quotient
+                s_out = float(w0["output_scale"][0])
+                codes = w0["out"].cpu()[tuple(torch.as_tensor(x) for x in pos)]
+                got = codes.view(torch.float8_e4m3fn).double().numpy()
+                q = np.clip(ref[wr] / s_out, -448, 448)
+                step = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(q), 2.0 ** -6))) - 3)
+                ok = bool(np.all(np.abs(got[wr] - q) <= step + tol / s_out))
+            else:
+                got = w0["out"].float().cpu().double().numpy()[tuple(pos)]
+                ok = bool(np.all(np.abs(got[wr] - ref[wr]) <= tol))
             spot = {"elements": int(wr.sum()), "within_tolerance": ok}
 
     if rank == 0:

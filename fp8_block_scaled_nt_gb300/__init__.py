@@ -39,7 +39,7 @@ OK, ERR_INVALID_ARGUMENT, ERR_UNSUPPORTED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = ran
 STATUS_NAMES = {0: "FP8G_OK", 1: "FP8G_ERR_INVALID_ARGUMENT", 2: "FP8G_ERR_UNSUPPORTED",
                 3: "FP8G_ERR_ARCH", 4: "FP8G_ERR_CUDA", 5: "FP8G_ERR_TIMEOUT"}
 SCALE_K_MAJOR, SCALE_MN_MAJOR = 0, 1
-OUT_BF16, OUT_F16 = 0, 1
+OUT_BF16, OUT_F16, OUT_E4M3 = 0, 1, 2
 DEVICE_TIMEOUT, DEVICE_BAD_M_INDICES, DEVICE_MASKED_M_CLAMPED = 0x1, 0x2, 0x4
 
 
@@ -62,7 +62,7 @@ def load():
                            "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
     lib = ctypes.CDLL(LIB_PATH)
     P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-    lib.fp8_gemm_nt_groupwise.argtypes = [P, P, P, P, P, I, I64, I64, I64, I, I, I, I, I, P]
+    lib.fp8_gemm_nt_groupwise.argtypes = [P, P, P, P, P, I, P, I64, I64, I64, I, I, I, I, I, P]
     lib.fp8_group_gemm_contiguous.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, P]
     lib.fp8_batch_gemm_masked.argtypes = [P, P, P, P, P, I64, P, I64, I64, I64, I64, P]
     lib.fp8g_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
@@ -144,7 +144,9 @@ def _out_code(dtype):
         return OUT_BF16
     if dtype == torch.float16:
         return OUT_F16
-    raise TypeError("output dtype must be bfloat16 or float16, got %s" % dtype)
+    if dtype in (torch.float8_e4m3fn, torch.uint8):
+        return OUT_E4M3
+    raise TypeError("output dtype must be bfloat16, float16 or float8_e4m3fn, got %s" % dtype)
 
 
 def _check_granularity(g):
@@ -156,9 +158,19 @@ def _check_granularity(g):
 # ------------------------------------------------------------- C entry points
 
 def fp8_gemm_nt_groupwise(a, b, a_scale, b_scale, out, scale_major="K", mma_sm=1,
-                          scale_granularity_mnk=(1, 128, 128), stream=None):
-    """out (m,n) = a (m,k) @ b (n,k).T with groupwise scales; returns out."""
+                          scale_granularity_mnk=(1, 128, 128), stream=None, output_scale=None):
+    """out (m,n) = a (m,k) @ b (n,k).T with groupwise scales; returns out.
+
+    ``out`` is BF16/FP16, or E4M3 (``float8_e4m3fn`` or ``uint8`` codes) together
+    with ``output_scale``, a one-element float32 device tensor s: out = E4M3(R / s).
+    """
     torch = _torch()
+    code = _out_code(out.dtype)
+    _need((code == OUT_E4M3) == (output_scale is not None),
+          "output_scale goes with (and only with) an E4M3 out")
+    if output_scale is not None:
+        _need(output_scale.dtype == torch.float32 and output_scale.numel() == 1,
+              "output_scale must be a one-element float32 tensor")
     _e4m3(a, "a"), _e4m3(b, "b")
     _need(a.dim() == 2 and b.dim() == 2 and out.dim() == 2, "a, b, out must be 2-D")
     m, k = a.shape
@@ -177,10 +189,11 @@ def fp8_gemm_nt_groupwise(a, b, a_scale, b_scale, out, scale_major="K", mma_sm=1
         _need(tuple(b_scale.shape) == (kb, nb), "MN-major b_scale must be (%d, %d)" % (kb, nb))
     else:
         raise ValueError("scale_major must be 'K', 'MN' or None")
-    dev = _cuda_contig((a, b, a_scale, b_scale, out), ("a", "b", "a_scale", "b_scale", "out"))
+    dev = _cuda_contig((a, b, a_scale, b_scale, out, output_scale),
+                       ("a", "b", "a_scale", "b_scale", "out", "output_scale"))
     g = tuple(scale_granularity_mnk)
     rc = load().fp8_gemm_nt_groupwise(
-        _ptr(a), _ptr(b), _ptr(a_scale), _ptr(b_scale), _ptr(out), _out_code(out.dtype),
+        _ptr(a), _ptr(b), _ptr(a_scale), _ptr(b_scale), _ptr(out), code, _ptr(output_scale),
         m, n, k, sm, g[0], g[1], g[2], int(mma_sm), _stream_handle(stream, dev))
     _raise_on(rc, "fp8_gemm_nt_groupwise")
     return out
@@ -269,18 +282,16 @@ def gemm_fp8_nt_groupwise(a, b, a_scale, b_scale, scale_major_mode=None, mma_sm=
                           backend="auto", output_scale=None):
     """The page's ``gemm_fp8_nt_groupwise``: returns out (m, n)."""
     torch = _torch()
-    if output_scale is not None:
-        raise Fp8gError(ERR_UNSUPPORTED, "gemm_fp8_nt_groupwise",
-                        "FP8 output with output_scale is not provided")
     if backend != "auto":
         raise Fp8gError(ERR_UNSUPPORTED, "gemm_fp8_nt_groupwise",
                         "only backend='auto' (this library's sm_103a kernel) exists")
     _check_granularity(scale_granularity_mnk)
     if out is None:
+        default = torch.float8_e4m3fn if output_scale is not None else torch.bfloat16
         out = torch.empty((a.shape[0], b.shape[0]), device=a.device,
-                          dtype=out_dtype if out_dtype is not None else torch.bfloat16)
+                          dtype=out_dtype if out_dtype is not None else default)
     return fp8_gemm_nt_groupwise(a, b, a_scale, b_scale, out, scale_major_mode or "K", mma_sm,
-                                 scale_granularity_mnk)
+                                 scale_granularity_mnk, output_scale=output_scale)
 
 
 def group_deepgemm_fp8_nt_groupwise(a, b, a_scale, b_scale, m_indices,

@@ -44,8 +44,9 @@ fp8g_status_t cuda_fail(cudaError_t e, const char* what) {
 }
 
 constexpr int kMaxDevices = 64;
-// dense bf16, dense f16 (single CTA), grouped, masked, dense bf16, dense f16 (CTA pair)
-constexpr int kNumKernels = 6;
+// dense bf16, dense f16 (single CTA), grouped, masked, dense bf16, dense f16 (CTA pair),
+// dense E4M3 (single CTA), dense E4M3 (CTA pair)
+constexpr int kNumKernels = 8;
 
 struct DeviceState {
     bool probed = false;
@@ -241,14 +242,21 @@ const char* fp8g_last_error(void) { return t_last_error.c_str(); }
 
 fp8g_status_t fp8_gemm_nt_groupwise(const void* a, const void* b, const float* a_scale,
                                     const float* b_scale, void* out, fp8g_dtype_t out_dtype,
-                                    int64_t m, int64_t n, int64_t k, fp8g_scale_major_t scale_major,
+                                    const float* output_scale, int64_t m, int64_t n, int64_t k,
+                                    fp8g_scale_major_t scale_major,
                                     int gran_m, int gran_n, int gran_k, int mma_sm,
                                     cudaStream_t stream) {
     try {
         if (m < 0) return fail(FP8G_ERR_INVALID_ARGUMENT, "m = %lld < 0", (long long)m);
-        if (out_dtype != FP8G_OUT_BF16 && out_dtype != FP8G_OUT_F16)
-            return fail(FP8G_ERR_INVALID_ARGUMENT, "out_dtype %d is neither BF16 nor FP16",
+        if (out_dtype != FP8G_OUT_BF16 && out_dtype != FP8G_OUT_F16 &&
+            out_dtype != FP8G_OUT_E4M3)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "out_dtype %d is not BF16, FP16 or E4M3",
                         (int)out_dtype);
+        if ((out_dtype == FP8G_OUT_E4M3) != (output_scale != nullptr))
+            return fail(FP8G_ERR_INVALID_ARGUMENT,
+                        "output_scale must be given exactly when out_dtype is E4M3");
+        if (output_scale && !aligned(output_scale, 4))
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "output_scale must be 4-byte aligned");
         if (scale_major != FP8G_SCALE_K_MAJOR && scale_major != FP8G_SCALE_MN_MAJOR)
             return fail(FP8G_ERR_INVALID_ARGUMENT, "scale_major %d is neither K nor MN",
                         (int)scale_major);
@@ -287,7 +295,13 @@ fp8g_status_t fp8_gemm_nt_groupwise(const void* a, const void* b, const float* a
         p.num_tiles = static_cast<int>(tiles);
         p.num_groups = 1;
         p.scale_mn_major = scale_major == FP8G_SCALE_MN_MAJOR;
+        p.out_scale = output_scale;
         p.status = ds->status;
+        if (out_dtype == FP8G_OUT_E4M3)
+            return pair ? launch<fp8g::FORM_DENSE, __nv_fp8_e4m3, true>(*ds, 7, map_a, map_b, p,
+                                                                        tiles, stream)
+                        : launch<fp8g::FORM_DENSE, __nv_fp8_e4m3, false>(*ds, 6, map_a, map_b, p,
+                                                                         tiles, stream);
         if (out_dtype == FP8G_OUT_BF16)
             return pair ? launch<fp8g::FORM_DENSE, __nv_bfloat16, true>(*ds, 4, map_a, map_b, p,
                                                                         tiles, stream)

@@ -45,6 +45,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <limits.h>
 #include <stdint.h>
 
@@ -110,6 +111,7 @@ struct Params {
     int num_tiles;         // dense/grouped: m_blocks * n_tiles
     int num_groups;
     int scale_mn_major;  // dense form only
+    const float* out_scale;  // dense form with E4M3 output: the output's FP32 scale
     int band_m;          // m-blocks per raster band (dense/grouped)
 };
 
@@ -442,10 +444,20 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, __half*) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
 }
+// Four E4M3 codes (first value in the low byte) of v * inv, rounded to nearest
+// even and saturated to +-448.
+__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d, float inv) {
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a * inv, b * inv), __NV_SATFINITE,
+                                                 __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c * inv, d * inv), __NV_SATFINITE,
+                                                 __NV_E4M3);
+    return lo | (hi << 16);
+}
 
 // Epilogue of one promotion warpgroup: its 128 rows x 128 columns of FP32
-// sums (thread r holds row r; acc[i] = columns 2i, 2i+1) go out in two passes
-// of 64 columns.  Each thread rounds its row segment into 128 bytes of shared
+// sums (thread r holds row r; acc[i] = columns 2i, 2i+1) go out in 128-byte
+// row segments: two passes of 64 columns for BF16/FP16, one pass of 128
+// columns for E4M3 codes (of value * out_inv).  Each thread rounds its row segment into 128 bytes of shared
 // memory (16-byte chunk c of row r at chunk c ^ (r % 8), so that the 32 rows
 // a warp writes at once spread over all banks); then each warp stores the 32
 // rows it owns as full 128-byte segments, four rows per instruction, skipping
@@ -453,22 +465,40 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, __half*) {
 template <typename OutT>
 __device__ __forceinline__ void store_tile_rows(OutT* out, int64_t n, int64_t row_base, int col0,
                                                 bool row_ok, const uint64_t (&acc)[64],
-                                                uint8_t* staging, uint32_t barrier_id) {
+                                                uint8_t* staging, uint32_t barrier_id,
+                                                float out_inv) {
+    constexpr int ESZ = static_cast<int>(sizeof(OutT));  // 2 (BF16/FP16) or 1 (E4M3)
+    constexpr int PASSES = ESZ;                          // 128 columns x ESZ bytes
+    constexpr int PASS_COLS = 128 / ESZ;
     const int lane = threadIdx.x & 31;
     const int quarter = (threadIdx.x >> 5) & 3;
     const int r = quarter * 32 + lane;
     const uint32_t base = smem_u32(staging);
     OutT* tag = nullptr;
+    (void)tag;
+    (void)out_inv;
 #pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {
+    for (int pass = 0; pass < PASSES; ++pass) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            const int a = pass * 32 + 4 * c;
             uint4 v;
-            v.x = pack2(lo_f32(acc[a + 0]), hi_f32(acc[a + 0]), tag);
-            v.y = pack2(lo_f32(acc[a + 1]), hi_f32(acc[a + 1]), tag);
-            v.z = pack2(lo_f32(acc[a + 2]), hi_f32(acc[a + 2]), tag);
-            v.w = pack2(lo_f32(acc[a + 3]), hi_f32(acc[a + 3]), tag);
+            if constexpr (ESZ == 2) {
+                const int a = pass * 32 + 4 * c;  // 8 values
+                v.x = pack2(lo_f32(acc[a + 0]), hi_f32(acc[a + 0]), tag);
+                v.y = pack2(lo_f32(acc[a + 1]), hi_f32(acc[a + 1]), tag);
+                v.z = pack2(lo_f32(acc[a + 2]), hi_f32(acc[a + 2]), tag);
+                v.w = pack2(lo_f32(acc[a + 3]), hi_f32(acc[a + 3]), tag);
+            } else {
+                const int a = 8 * c;  // 16 values
+                v.x = pack4_e4m3(lo_f32(acc[a + 0]), hi_f32(acc[a + 0]), lo_f32(acc[a + 1]),
+                                 hi_f32(acc[a + 1]), out_inv);
+                v.y = pack4_e4m3(lo_f32(acc[a + 2]), hi_f32(acc[a + 2]), lo_f32(acc[a + 3]),
+                                 hi_f32(acc[a + 3]), out_inv);
+                v.z = pack4_e4m3(lo_f32(acc[a + 4]), hi_f32(acc[a + 4]), lo_f32(acc[a + 5]),
+                                 hi_f32(acc[a + 5]), out_inv);
+                v.w = pack4_e4m3(lo_f32(acc[a + 6]), hi_f32(acc[a + 6]), lo_f32(acc[a + 7]),
+                                 hi_f32(acc[a + 7]), out_inv);
+            }
             st_shared_v4(base + r * 128 + ((c ^ (r & 7)) << 4), v);
         }
         named_barrier_sync(barrier_id, 128);
@@ -480,8 +510,8 @@ __device__ __forceinline__ void store_tile_rows(OutT* out, int64_t n, int64_t ro
             const bool ok_i = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, i) != 0;
             const uint4 v = ld_shared_v4(base + rr * 128 + ((chunk ^ (rr & 7)) << 4));
             if (ok_i)
-                *reinterpret_cast<uint4*>(out + (row_base + rr) * n + col0 + pass * OUT_COLS +
-                                          chunk * 8) = v;
+                *reinterpret_cast<uint4*>(out + (row_base + rr) * n + col0 + pass * PASS_COLS +
+                                          chunk * (16 / ESZ)) = v;
         }
         named_barrier_sync(barrier_id, 128);  // staging free for the next pass
     }
@@ -503,6 +533,9 @@ __device__ __forceinline__ void run_promotion(const Params& p, int rank, uint64_
     const int KB = p.kblocks;
     OutT* out = static_cast<OutT*>(p.out);
     Scheduler<FORM, PAIR> sched(p, rank);
+    // E4M3 output: codes of value / out_scale, computed as value * (1 / out_scale)
+    float out_inv = 1.0f;
+    if constexpr (sizeof(OutT) == 1) out_inv = __frcp_rn(__ldg(p.out_scale));
     // A pair's TMEM buffers are released on the even CTA, whose MMA warp reuses them.
     uint32_t release0 = 0, release1 = 0;
     if constexpr (PAIR) {
@@ -610,7 +643,7 @@ __device__ __forceinline__ void run_promotion(const Params& p, int rank, uint64_
         // after an abort (then storing nothing); the warpgroup stops together.
         if (col_ok)  // uniform over the warpgroup
             store_tile_rows<OutT>(out, p.n, out_row - r, col0, ok && row_ok, acc,
-                                  sOut + half * OUT_STAGE_BYTES, 1 + half);
+                                  sOut + half * OUT_STAGE_BYTES, 1 + half, out_inv);
         if (named_barrier_or(1 + half, 128, !ok)) break;
     }
 }

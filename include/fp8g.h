@@ -62,8 +62,9 @@ typedef enum {
  *   MN-major: a_scale (k/128, m),   b_scale (k/128, n/128)              */
 typedef enum { FP8G_SCALE_K_MAJOR = 0, FP8G_SCALE_MN_MAJOR = 1 } fp8g_scale_major_t;
 
-/* Output element type: BF16 (the page's default) or FP16. */
-typedef enum { FP8G_OUT_BF16 = 0, FP8G_OUT_F16 = 1 } fp8g_dtype_t;
+/* Output element type: BF16 (the page's default), FP16, or E4M3 codes with a
+ * per-tensor FP32 output scale (the page's output_scale path). */
+typedef enum { FP8G_OUT_BF16 = 0, FP8G_OUT_F16 = 1, FP8G_OUT_E4M3 = 2 } fp8g_dtype_t;
 
 /* Bits of the device status word (see fp8g_get_device_status). */
 #define FP8G_DEVICE_TIMEOUT 0x1u          /* a pipeline wait exceeded its limit; the launch gave up */
@@ -77,8 +78,13 @@ typedef enum { FP8G_OUT_BF16 = 0, FP8G_OUT_F16 = 1 } fp8g_dtype_t;
  *   b        (n, k)  E4M3 codes, row-major; the operation is a @ b.T.
  *   a_scale  FP32, (m, k/128) if K-major, (k/128, m) if MN-major.
  *   b_scale  FP32, (n/128, k/128) if K-major, (k/128, n/128) if MN-major.
- *   out      (m, n) row-major, BF16 or FP16 per out_dtype.  Every element is
- *            written.
+ *   out      (m, n) row-major, BF16, FP16 or E4M3 per out_dtype.  Every
+ *            element is written.
+ *   output_scale  NULL for BF16/FP16 output.  For FP8G_OUT_E4M3 (and only
+ *            then) a device pointer to one FP32 value s > 0, the scale of the
+ *            FP8 output in the same sense as a_scale and b_scale (value =
+ *            code * s): out = E4M3(R * (1/s)) with R the FP32 result, 1/s
+ *            correctly rounded, round to nearest even, saturated to +-448.
  *   gran_m, gran_n, gran_k   the page's scale_granularity_mnk; only
  *            (1, 128, 128) is provided, anything else is FP8G_ERR_UNSUPPORTED.
  *   mma_sm   the page's MMA configuration hint: 0 (auto), 1 or 2.  It may
@@ -87,6 +93,7 @@ typedef enum { FP8G_OUT_BF16 = 0, FP8G_OUT_F16 = 1 } fp8g_dtype_t;
 fp8g_status_t fp8_gemm_nt_groupwise(const void* a, const void* b,
                                     const float* a_scale, const float* b_scale,
                                     void* out, fp8g_dtype_t out_dtype,
+                                    const float* output_scale,
                                     int64_t m, int64_t n, int64_t k,
                                     fp8g_scale_major_t scale_major,
                                     int gran_m, int gran_n, int gran_k,

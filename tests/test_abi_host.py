@@ -53,9 +53,9 @@ def test_header_compiles_as_c():
         assert r.returncode == 0, r.stderr
 
 
-def _dense(h, a=16, b=16, sa=16, sb=16, out=16, dt=0, m=128, n=256, k=256, major=0,
+def _dense(h, a=16, b=16, sa=16, sb=16, out=16, dt=0, os_=None, m=128, n=256, k=256, major=0,
            gran=(1, 128, 128), mma_sm=1):
-    return h.fp8_gemm_nt_groupwise(a, b, sa, sb, out, dt, m, n, k, major, gran[0], gran[1],
+    return h.fp8_gemm_nt_groupwise(a, b, sa, sb, out, dt, os_, m, n, k, major, gran[0], gran[1],
                                    gran[2], mma_sm, None)
 
 
@@ -73,6 +73,9 @@ def _dense(h, a=16, b=16, sa=16, sb=16, out=16, dt=0, m=128, n=256, k=256, major
     (dict(b=24), 1, "16-byte"),
     (dict(sa=18), 1, "4-byte"),
     (dict(n=1 << 31), 2, "2^31"),
+    (dict(dt=2), 1, "output_scale"),
+    (dict(os_=16), 1, "output_scale"),
+    (dict(dt=2, os_=18), 1, "4-byte"),
 ])
 def test_dense_host_validation(lib, kwargs, status, msg):
     h = lib.load()

@@ -217,14 +217,125 @@ def test_invalid_arguments_launch_nothing(fp8g):
     lib = fp8g.load()
     # k not a multiple of 128, straight through the C ABI
     rc = lib.fp8_gemm_nt_groupwise(w["a"].data_ptr(), w["b"].data_ptr(), w["a_scale"].data_ptr(),
-                                   w["b_scale"].data_ptr(), out.data_ptr(), 0, 128, 256, 200, 0,
-                                   1, 128, 128, 1, None)
+                                   w["b_scale"].data_ptr(), out.data_ptr(), 0, None, 128, 256, 200,
+                                   0, 1, 128, 128, 1, None)
     assert rc == fp8g.ERR_INVALID_ARGUMENT and "k = 200" in fp8g.last_error()
     # misaligned a
     rc = lib.fp8_gemm_nt_groupwise(w["a"].data_ptr() + 8, w["b"].data_ptr(),
                                    w["a_scale"].data_ptr(), w["b_scale"].data_ptr(),
-                                   out.data_ptr(), 0, 128, 256, 256, 0, 1, 128, 128, 1, None)
+                                   out.data_ptr(), 0, None, 128, 256, 256, 0, 1, 128, 128, 1, None)
     assert rc == fp8g.ERR_INVALID_ARGUMENT
     torch.cuda.synchronize()
     assert not written_rows(out).any()
     assert fp8g.get_device_status() == 0
+
+
+# ----------------------------------------------- FP8 (E4M3) output with output_scale
+
+def _decode_e4m3(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def _e4m3_step(q):
+    """Spacing of the E4M3 grid at |q| (2^-9 in the subnormal range)."""
+    e = np.floor(np.log2(np.maximum(np.abs(q), 2.0 ** -6)))
+    return 2.0 ** (e - 3)
+
+
+def _run_fp8_out(fp8g, w, s, mma_sm):
+    d = to_device(w)
+    os_ = torch.tensor([s], dtype=torch.float32, device="cuda")
+    out = torch.full((w["m"], w["n"]), 0x7F, dtype=torch.uint8, device="cuda")  # NaN sentinel
+    fp8g.fp8_gemm_nt_groupwise(d["a"], d["b"], d["a_scale"], d["b_scale"], out,
+                               scale_major=w["scale_major"], mma_sm=mma_sm, output_scale=os_)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("mma_sm", [1, 2])
+@pytest.mark.parametrize("mnk", [(200, 384, 384), (7, 256, 640), (520, 384, 1152), (129, 640, 256)])
+def test_fp8_output_parity(fp8g, oracle_mod, mnk, mma_sm):
+    m, n, k = mnk
+    w = workloads.dense(m, n, k, seed=m + 3 * n + k)
+    ref, _ = _oracle_full(oracle_mod, w, torch.bfloat16)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    s = float(np.float32(rms / 64))  # the bulk of |R| / s near 64, the largest values saturate
+    codes = _run_fp8_out(fp8g, w, s, mma_sm)
+    assert not np.any(codes == 0x7F)  # every element written, no NaN
+    q = np.clip(ref / s, -448, 448)
+    tol = (1e-2 * np.abs(ref) + 2e-3 * rms) / s
+    assert np.all(np.abs(_decode_e4m3(codes) - q) <= _e4m3_step(q) + tol)
+    want = oracle_mod.quantize_output_e4m3(ref, s)
+    assert np.mean(codes == want) > 0.99
+
+
+def test_fp8_output_closed_form_exact(fp8g, oracle_mod):
+    # a = b = 1, power-of-two block scales and output scale: R and R / s are
+    # exact in FP32, so every code is determined
+    m, n, k = 256, 512, 512
+    a = torch.full((m, k), 0x38, dtype=torch.uint8)
+    b = torch.full((n, k), 0x38, dtype=torch.uint8)
+    g = torch.Generator().manual_seed(8)
+    ea = torch.randint(-5, 3, (m, k // 128), generator=g).float()
+    eb = torch.randint(-5, 3, (n // 128, k // 128), generator=g).float()
+    w = dict(a=a, b=b, a_scale=torch.exp2(ea), b_scale=torch.exp2(eb), m=m, n=n, k=k,
+             scale_major="K")
+    ref, _ = _oracle_full(oracle_mod, w, torch.bfloat16)
+    for mma_sm in (1, 2):
+        for s in (0.25, 1.0, 2.0):
+            codes = _run_fp8_out(fp8g, w, s, mma_sm)
+            assert np.array_equal(codes, oracle_mod.quantize_output_e4m3(ref, s)), (mma_sm, s)
+
+
+def test_fp8_output_scale_doubling_halves_values_exactly(fp8g):
+    w = workloads.dense(384, 512, 768, seed=98)
+    c1 = _decode_e4m3(_run_fp8_out(fp8g, w, 0.05, 2))
+    c2 = _decode_e4m3(_run_fp8_out(fp8g, w, 0.1, 2))
+    normal = (np.abs(c1) >= 2.0 ** -5) & (np.abs(c1) < 448)  # away from subnormals and saturation
+    assert normal.mean() > 0.5
+    assert np.array_equal(c2[normal] * 2, c1[normal])
+
+
+def test_fp8_output_page_signature(fp8g, oracle_mod):
+    w = workloads.dense(256, 256, 512, seed=99)
+    d = to_device(w)
+    os_ = torch.tensor([0.02], dtype=torch.float32, device="cuda")
+    out = fp8g.gemm_fp8_nt_groupwise(d["a"].view(torch.float8_e4m3fn),
+                                     d["b"].view(torch.float8_e4m3fn), d["a_scale"], d["b_scale"],
+                                     output_scale=os_)
+    assert out.dtype == torch.float8_e4m3fn and out.shape == (256, 256)
+    ref, _ = _oracle_full(oracle_mod, w, torch.bfloat16)
+    q = np.clip(ref / float(os_.item()), -448, 448)
+    got = out.cpu().view(torch.uint8).numpy()
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    tol = (1e-2 * np.abs(ref) + 2e-3 * rms) / float(os_.item())
+    assert np.all(np.abs(_decode_e4m3(got) - q) <= _e4m3_step(q) + tol)
+
+
+def test_fp8_output_4096x7168x2048_sampled(fp8g, oracle_mod):
+    w = workloads.make("dense_4096x7168x2048_e4m3out")
+    s = float(w["output_scale"][0])
+    codes = _run_fp8_out(fp8g, w, s, 0)  # the launch configuration bench.py times
+    r, c = workloads.sample_positions(w["m"], w["n"], 65536, seed=13, extra_rows=(0, w["m"] - 1))
+    ref, _ = oracle_mod.gemm_nt_groupwise_at(w["a"], w["b"], w["a_scale"], w["b_scale"], r, c)
+    got = codes[r.numpy(), c.numpy()]
+    q = np.clip(ref / s, -448, 448)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    tol = (1e-2 * np.abs(ref) + 2e-3 * rms) / s
+    assert np.all(np.abs(_decode_e4m3(got) - q) <= _e4m3_step(q) + tol)
+    assert np.mean(got == oracle_mod.quantize_output_e4m3(ref, s)) > 0.99
+
+
+def test_fp8_output_argument_errors(fp8g):
+    w = to_device(workloads.dense(128, 256, 256, seed=100))
+    out8 = torch.zeros((128, 256), dtype=torch.uint8, device="cuda")
+    with pytest.raises(ValueError):  # E4M3 out without output_scale
+        fp8g.fp8_gemm_nt_groupwise(w["a"], w["b"], w["a_scale"], w["b_scale"], out8)
+    lib = fp8g.load()
+    os_ = torch.ones(1, dtype=torch.float32, device="cuda")
+    rc = lib.fp8_gemm_nt_groupwise(w["a"].data_ptr(), w["b"].data_ptr(), w["a_scale"].data_ptr(),
+                                   w["b_scale"].data_ptr(), out8.data_ptr(), 0, os_.data_ptr(),
+                                   128, 256, 256, 0, 1, 128, 128, 1, None)
+    assert rc == fp8g.ERR_INVALID_ARGUMENT and "output_scale" in fp8g.last_error()
+    torch.cuda.synchronize()
+    assert not out8.any()

@@ -29,6 +29,12 @@ CONFIGS = {
                               scale_exp=(-4.0, 2.0), out_dtype="bf16", seed=1001),
     "dense_4096x7168x2048": dict(kind="dense", m=4096, n=7168, k=2048, dist="normal",
                                  scale_exp=(-6.0, 0.0), out_dtype="bf16", seed=1002),
+    # the same GEMM with FP8 (E4M3) output and a per-tensor output scale; with
+    # these inputs R has an RMS near 5.4, so R / s (RMS ~87) spans the E4M3
+    # range and under 0.1% of the outputs saturate
+    "dense_4096x7168x2048_e4m3out": dict(kind="dense", m=4096, n=7168, k=2048, dist="normal",
+                                         scale_exp=(-6.0, 0.0), out_dtype="e4m3",
+                                         output_scale=0.0625, seed=1007),
     "grouped_4096tok_top8_e64_n4096_k7168": dict(
         kind="grouped", num_tokens=4096, top_k=8, num_experts=64, n=4096, k=7168,
         scale_exp=(-6.0, 0.0), seed=1003),
@@ -82,8 +88,9 @@ def log_uniform(shape, lo, hi, gen, device="cpu"):
 
 
 def dense(m, n, k, seed, dist="normal", scale_exp=(-6.0, 0.0), scale_major="K",
-          device="cpu", **_):
-    """a (m,k), b (n,k) E4M3 codes; scales in the requested layout."""
+          device="cpu", output_scale=None, **_):
+    """a (m,k), b (n,k) E4M3 codes; scales in the requested layout; with
+    `output_scale`, also the one-element FP32 scale of an E4M3 output."""
     gen = generator(seed, device)
     kb, nb = k // KBLOCK, n // NBLOCK
     a = _draw((m, k), dist, gen, device)
@@ -94,8 +101,10 @@ def dense(m, n, k, seed, dist="normal", scale_exp=(-6.0, 0.0), scale_major="K",
         sa, sb = sa.t().contiguous(), sb.t().contiguous()
     elif scale_major != "K":
         raise ValueError(scale_major)
-    return dict(a=a, b=b, a_scale=sa, b_scale=sb, m=m, n=n, k=k,
-                scale_major=scale_major)
+    d = dict(a=a, b=b, a_scale=sa, b_scale=sb, m=m, n=n, k=k, scale_major=scale_major)
+    if output_scale is not None:
+        d["output_scale"] = torch.tensor([output_scale], dtype=torch.float32, device=device)
+    return d
 
 
 def routing_m_indices(num_tokens, top_k, num_experts, gen, align=128):
