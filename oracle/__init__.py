@@ -9,7 +9,8 @@ only marshals numpy arrays (or CPU torch tensors) into it.  It follows the MATE
 page "FlashInfer Wrapper APIs", section GEMM: ``gemm_fp8_nt_groupwise``,
 ``group_deepgemm_fp8_nt_groupwise`` and ``batch_deepgemm_fp8_nt_groupwise``;
 and section Norm: ``fused_add_rmsnorm_fp8_block_quant`` (the producer of the
-GEMM's FP8 activations and their 1 x 128 scales).
+GEMM's FP8 activations and their 1 x 128 scales); and the DeepSeek FP8
+block-scale MoE layer of the "flashinfer-rs" page built from the grouped GEMM.
 """
 import ctypes
 
@@ -51,8 +52,13 @@ def _load():
         lib.oracle_e4m3_encode.restype = None
         lib.oracle_fused_add_rmsnorm_fp8_block_quant.argtypes = [
             P, P, P, ctypes.c_double, I64, I64, P, P, P, P]
+        lib.oracle_quant_1x128.argtypes = [P, I64, I64, P, P]
+        lib.oracle_quant_1x128.restype = None
+        lib.oracle_moe_deepseek_fp8_block_scale.argtypes = [P, P, P, P, P, P, I64, I64, I64,
+                                                            I64, I64, P]
         for f in ("oracle_gemm_nt_groupwise", "oracle_gemm_nt_groupwise_at",
                   "oracle_fused_add_rmsnorm_fp8_block_quant",
+                  "oracle_moe_deepseek_fp8_block_scale",
                   "oracle_group_gemm_contiguous", "oracle_group_gemm_contiguous_at",
                   "oracle_batch_gemm_masked", "oracle_batch_gemm_masked_at",
                   "oracle_num_threads"):
@@ -261,3 +267,42 @@ def quantize_output_e4m3(ref, output_scale):
     and b_scale do."""
     r = np.asarray(ref, np.float64)
     return e4m3_encode(r / float(np.float32(output_scale)))
+
+
+def quant_1x128(x):
+    """Row-major 1 x 128 E4M3 quantisation of FP64 values (rows, cols):
+    returns (codes uint8 (rows, cols), scales float32 (rows, cols // 128))."""
+    x = _arr(x, np.float64)
+    rows, cols = x.shape
+    if cols % 128:
+        raise ValueError("cols must be a multiple of 128")
+    codes = np.empty((rows, cols), np.uint8)
+    scales = np.empty((rows, cols // 128), np.float32)
+    _load().oracle_quant_1x128(x.ctypes.data, rows, cols, codes.ctypes.data, scales.ctypes.data)
+    return codes, scales
+
+
+def moe_deepseek_fp8_block_scale(input_bits, token_selected, w1, w2, s1, s2):
+    """DeepSeek FP8 block-scale MoE layer (see oracle.h): BF16 input
+    encodings (tokens, hidden), int32 token_selected (tokens, top_k), E4M3
+    fc1 (E, 2*inter, hidden) and fc2 (E, hidden, inter) with their FP32 block
+    scales.  Returns the BF16 encodings of out (tokens, hidden)."""
+    x = _arr(input_bits, np.uint16)
+    ts = _arr(token_selected, np.int32)
+    w1, w2 = _arr(w1, np.uint8), _arr(w2, np.uint8)
+    s1, s2 = _arr(s1, np.float32), _arr(s2, np.float32)
+    tokens, hidden = x.shape
+    top_k = ts.shape[1]
+    e, two_i, h2 = w1.shape
+    inter = two_i // 2
+    if h2 != hidden or w2.shape != (e, hidden, inter) or ts.shape[0] != tokens:
+        raise ValueError("shape mismatch")
+    if s1.shape != (e, two_i // 128, hidden // 128) or s2.shape != (e, hidden // 128, inter // 128):
+        raise ValueError("scale shape mismatch")
+    out = np.empty((tokens, hidden), np.uint16)
+    rc = _load().oracle_moe_deepseek_fp8_block_scale(
+        _p(x), _p(ts), _p(w1), _p(w2), _p(s1), _p(s2), tokens, e, top_k, hidden, inter, _p(out))
+    if rc == -2:
+        raise ValueError("moe: token_selected holds an expert id outside [-1, num_experts)")
+    _check(rc, "moe_deepseek_fp8_block_scale")
+    return out

@@ -14,6 +14,7 @@
 #include "oracle.h"
 
 #include <math.h>
+#include <stdlib.h>
 #include <stddef.h>
 
 #ifdef _OPENMP
@@ -500,6 +501,38 @@ static double bf16_value(uint16_t bits)
     return (double)v.f;
 }
 
+/* Row-major 1 x 128 FP8 quantisation of `cols` values: per block of 128,
+ * scale = FP32(amax / 448) and code = E4M3(FP32(x / scale)) (an FP64 quotient
+ * of two FP32 values rounded to FP32 is the correctly rounded FP32 quotient);
+ * an all-zero block gets scale 0 and codes 0. */
+static void quant_row_1x128(const double* x, int64_t cols, uint8_t* codes, float* scales)
+{
+    for (int64_t b = 0; b < cols / KBLOCK; ++b) {
+        double amax = 0.0;
+        for (int64_t j = b * KBLOCK; j < (b + 1) * KBLOCK; ++j)
+            if (fabs(x[j]) > amax)
+                amax = fabs(x[j]);
+        float scale = (float)(amax / 448.0);
+        scales[b] = scale;
+        for (int64_t j = b * KBLOCK; j < (b + 1) * KBLOCK; ++j) {
+            double q = 0.0;
+            if (amax > 0.0)
+                q = (double)(float)(x[j] / (double)scale);
+            oracle_e4m3_encode(&q, 1, &codes[j]);
+        }
+    }
+}
+
+void oracle_quant_1x128(const double* x, int64_t rows, int64_t cols, uint8_t* codes,
+                        float* scales)
+{
+    if (cols % KBLOCK)
+        return;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < rows; ++i)
+        quant_row_1x128(x + i * cols, cols, codes + i * cols, scales + i * (cols / KBLOCK));
+}
+
 int oracle_fused_add_rmsnorm_fp8_block_quant(const uint16_t* input,
                                              const uint16_t* residual,
                                              const uint16_t* weight, double eps,
@@ -525,28 +558,90 @@ int oracle_fused_add_rmsnorm_fp8_block_quant(const uint16_t* input,
             ss += x * x;
         }
         double r = 1.0 / sqrt(ss / (double)hidden + eps);
+        double* y = (double*)malloc(sizeof(double) * (size_t)hidden);
         for (int64_t j = 0; j < hidden; ++j) {
             double x = bf16_value(rout[j]);
-            round_one(x * r * bf16_value(weight[j]), ORACLE_OUT_BF16, &nout[j]);
+            y[j] = round_one(x * r * bf16_value(weight[j]), ORACLE_OUT_BF16, &nout[j]);
         }
-        for (int64_t b = 0; b < nblk; ++b) {
-            double amax = 0.0;
-            for (int64_t j = b * KBLOCK; j < (b + 1) * KBLOCK; ++j) {
-                double y = fabs(bf16_value(nout[j]));
-                if (y > amax)
-                    amax = y;
+        quant_row_1x128(y, hidden, out + i * hidden, block_scale + i * nblk);
+        free(y);
+    }
+    return 0;
+}
+
+/* ------------------------------------------- DeepSeek FP8 block-scale MoE */
+
+/* One GEMV row of the groupwise definition: sum over K blocks of the exact
+ * block sum times (x_scale[kb] * w_scale[kb]); w is one row of k codes. */
+static double block_scaled_dot(const double* dec, const uint8_t* xq, const float* xs,
+                               const uint8_t* w, const float* ws, int64_t k)
+{
+    double r = 0.0;
+    for (int64_t kb = 0; kb < k / KBLOCK; ++kb) {
+        double p = 0.0;
+        for (int64_t t = kb * KBLOCK; t < (kb + 1) * KBLOCK; ++t)
+            p += dec[xq[t]] * dec[w[t]];
+        r += p * ((double)xs[kb] * (double)ws[kb]);
+    }
+    return r;
+}
+
+int oracle_moe_deepseek_fp8_block_scale(const uint16_t* input, const int32_t* token_selected,
+                                        const uint8_t* w1, const uint8_t* w2,
+                                        const float* s1, const float* s2, int64_t num_tokens,
+                                        int64_t num_experts, int64_t top_k, int64_t hidden,
+                                        int64_t inter, uint16_t* out)
+{
+    if (num_tokens < 0 || num_experts <= 0 || top_k <= 0 || hidden <= 0 || inter <= 0 ||
+        hidden % KBLOCK || inter % KBLOCK)
+        return -1;
+    for (int64_t p = 0; p < num_tokens * top_k; ++p)
+        if (token_selected[p] < -1 || token_selected[p] >= num_experts)
+            return -2;
+    const int64_t hb = hidden / KBLOCK, ib = inter / KBLOCK;
+    double dec[256];
+    oracle_e4m3_table(dec);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        double* x = (double*)malloc(sizeof(double) * (size_t)hidden);
+        uint8_t* xq = (uint8_t*)malloc((size_t)hidden);
+        float* xs = (float*)malloc(sizeof(float) * (size_t)hb);
+        double* h = (double*)malloc(sizeof(double) * (size_t)(2 * inter));
+        double* act = (double*)malloc(sizeof(double) * (size_t)inter);
+        uint8_t* aq = (uint8_t*)malloc((size_t)inter);
+        float* as = (float*)malloc(sizeof(float) * (size_t)ib);
+        double* acc = (double*)calloc((size_t)hidden, sizeof(double));
+        /* the token's activations, quantised 1 x 128 */
+        for (int64_t j = 0; j < hidden; ++j)
+            x[j] = bf16_value(input[t * hidden + j]);
+        quant_row_1x128(x, hidden, xq, xs);
+        for (int64_t s = 0; s < top_k; ++s) {
+            const int64_t e = token_selected[t * top_k + s];
+            if (e < 0)
+                continue;
+            /* fc1 -> BF16; rows [0, inter) of the expert's fc1 are the gate,
+             * rows [inter, 2 inter) the up projection */
+            for (int64_t j = 0; j < 2 * inter; ++j) {
+                const uint8_t* wr = w1 + (e * 2 * inter + j) * hidden;
+                const float* sr = s1 + (e * (2 * inter / KBLOCK) + j / KBLOCK) * hb;
+                h[j] = round_one(block_scaled_dot(dec, xq, xs, wr, sr, hidden), ORACLE_OUT_BF16,
+                                 NULL);
             }
-            /* FP32 quotients: an FP64 quotient of two FP32 values rounded to
-             * FP32 is the correctly rounded FP32 quotient */
-            float scale = (float)(amax / 448.0);
-            block_scale[i * nblk + b] = scale;
-            for (int64_t j = b * KBLOCK; j < (b + 1) * KBLOCK; ++j) {
-                double q = 0.0;
-                if (amax > 0.0)
-                    q = (double)(float)(bf16_value(nout[j]) / (double)scale);
-                oracle_e4m3_encode(&q, 1, &out[i * hidden + j]);
+            /* SwiGLU: silu(gate) * up, silu(g) = g / (1 + e^-g) */
+            for (int64_t j = 0; j < inter; ++j)
+                act[j] = h[j] / (1.0 + exp(-h[j])) * h[inter + j];
+            quant_row_1x128(act, inter, aq, as);
+            /* fc2 -> BF16, summed over the token's experts */
+            for (int64_t j = 0; j < hidden; ++j) {
+                const uint8_t* wr = w2 + (e * hidden + j) * inter;
+                const float* sr = s2 + (e * hb + j / KBLOCK) * ib;
+                acc[j] += round_one(block_scaled_dot(dec, aq, as, wr, sr, inter),
+                                    ORACLE_OUT_BF16, NULL);
             }
         }
+        for (int64_t j = 0; j < hidden; ++j)
+            round_one(acc[j], ORACLE_OUT_BF16, &out[t * hidden + j]);
+        free(x); free(xq); free(xs); free(h); free(act); free(aq); free(as); free(acc);
     }
     return 0;
 }

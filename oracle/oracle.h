@@ -140,6 +140,36 @@ int oracle_fused_add_rmsnorm_fp8_block_quant(const uint16_t* input,
                                              uint16_t* normed_out, uint8_t* out,
                                              float* block_scale);
 
+/* Row-major 1 x 128 FP8 quantisation of FP64 values (rows, cols), cols a
+ * multiple of 128: per block scale = FP32(amax / 448), code = E4M3(FP32(x /
+ * scale)); an all-zero block gets scale 0 and codes 0.  codes (rows, cols),
+ * scales (rows, cols / 128). */
+void oracle_quant_1x128(const double* x, int64_t rows, int64_t cols, uint8_t* codes,
+                        float* scales);
+
+/* The DeepSeek FP8 block-scale MoE layer of the "flashinfer-rs" page, section
+ * "API Example: Fused MoE FP8 (cudarc)", DeepSeek FP8 block-scale mode, built
+ * from the groupwise GEMM of the MATE page, section GEMM.  For every token t:
+ *   (xq, xs) = 1x128 quantisation of input[t]                (BF16 -> E4M3)
+ *   for each of its top_k slots with expert e = token_selected[t, s] >= 0:
+ *     h   = BF16(fc1_e(xq))     fc1 (E, 2*inter, hidden) E4M3, scales s1
+ *                               (E, 2*inter/128, hidden/128); rows [0, inter)
+ *                               of h are the gate, [inter, 2*inter) the up part
+ *     act = silu(h_gate) * h_up                              (FP64)
+ *     (aq, as) = 1x128 quantisation of act
+ *     y   = BF16(fc2_e(aq))     fc2 (E, hidden, inter) E4M3, scales s2
+ *                               (E, hidden/128, inter/128)
+ *   out[t] = BF16(sum of y over the token's slots)           (unweighted)
+ * with fc(x)_j = sum_kb (block sum) * x_scale[kb] * w_scale[j/128][kb] as in the
+ * GEMM.  input and out are BF16 encodings (tokens, hidden); token_selected is
+ * (tokens, top_k) with -1 for an empty slot.  Returns -1 on a bad shape, -2 if
+ * an expert id lies outside [-1, num_experts). */
+int oracle_moe_deepseek_fp8_block_scale(const uint16_t* input, const int32_t* token_selected,
+                                        const uint8_t* w1, const uint8_t* w2,
+                                        const float* s1, const float* s2, int64_t num_tokens,
+                                        int64_t num_experts, int64_t top_k, int64_t hidden,
+                                        int64_t inter, uint16_t* out);
+
 /* Number of threads the oracle's parallel loops use. */
 int oracle_num_threads(void);
 
