@@ -187,6 +187,15 @@ def workload_stats(name, w):
     import workloads
     cfg = workloads.CONFIGS[name]
     kind = cfg["kind"]
+    if kind == "moe":
+        ts = w["token_selected"].cpu()
+        pairs = int((ts >= 0).sum())
+        live = int(torch_unique_count(ts[ts >= 0]))
+        hdim, inter, t = w["hidden"], w["inter"], w["tokens"]
+        flops = 2.0 * pairs * (2 * inter * hdim + hdim * inter)
+        # the live experts' weights and scales, the input and the output
+        bytes_ = live * (3 * inter * hdim + 4 * (3 * inter // 128) * (hdim // 128)) + 4 * t * hdim
+        return flops, bytes_, "tensor"
     if kind == "norm":
         rows, hidden = w["rows"], w["hidden"]
         # read input, residual; write residual, normed_out (BF16) and the codes
@@ -246,6 +255,14 @@ def make_sets(name, device):
             elif cfg["kind"] == "grouped":
                 w = workloads.make(name, device=device, seed=seed)
                 w["out"] = torch.empty((w["m"], w["n"]), dtype=torch.bfloat16, device=device)
+            elif cfg["kind"] == "moe":
+                import fp8_block_scaled_nt_gb300 as fp8g
+                w = workloads.make(name, device=device, seed=seed)
+                w["out"] = torch.empty((w["tokens"], w["hidden"]), dtype=torch.bfloat16,
+                                       device=device)
+                w["workspace"] = torch.empty(fp8g.moe_workspace_size(
+                    w["tokens"], w["num_experts"], w["top_k"], w["hidden"], w["inter"]),
+                    dtype=torch.uint8, device=device)
             elif cfg["kind"] == "norm":
                 w = workloads.make(name, device=device, seed=seed)
                 rows, hidden = w["rows"], w["hidden"]
@@ -283,6 +300,12 @@ def call_args(lib, name, w, stream_handle):
                 (p(w["a"]), p(w["b"]), p(w["a_scale"]), p(w["b_scale"]), p(w["out"]), od,
                  p(os_) if os_ is not None else None, w["m"], w["n"], w["k"], sm, 1, 128, 128, 0,
                  stream_handle))
+    if kind == "moe":
+        return (lib.fused_moe_deepseek_fp8_block_scale,
+                (p(w["input"]), p(w["token_selected"]), p(w["fc1"]), p(w["fc2"]), p(w["out"]),
+                 p(w["fc1_scale"]), p(w["fc2_scale"]), w["tokens"], w["num_experts"],
+                 w["top_k"], w["hidden"], w["inter"], p(w["workspace"]),
+                 w["workspace"].numel(), stream_handle))
     if kind == "norm":
         return (lib.fused_add_rmsnorm_fp8_block_quant,
                 (p(w["out"]), p(w["block_scale"]), p(w["normed_out"]), p(w["input"]),
@@ -313,6 +336,13 @@ def oracle_sample_rate(name, w, seconds, seed=21):
 
     def run(count):
         g = np.random.default_rng(seed)
+        if cfg["kind"] == "moe":
+            r = np.sort(g.choice(host["tokens"], size=min(count, host["tokens"]), replace=False))
+            t0 = time.perf_counter()
+            ref = oracle.moe_deepseek_fp8_block_scale(host["input"][r], host["token_selected"][r],
+                                                      host["fc1"], host["fc2"],
+                                                      host["fc1_scale"], host["fc2_scale"])
+            return time.perf_counter() - t0, r, ref, np.ones(r.size, bool)
         if cfg["kind"] == "norm":
             r = np.sort(g.choice(host["rows"], size=min(count, host["rows"]), replace=False))
             t0 = time.perf_counter()
@@ -352,6 +382,8 @@ def oracle_sample_rate(name, w, seconds, seed=21):
     # about `seconds` of oracle work
     if cfg["kind"] == "norm":
         count, limit = 4, host["rows"]
+    elif cfg["kind"] == "moe":
+        count, limit = 1, host["tokens"]
     else:
         count, limit = 4096, 50_000_000
     while True:
@@ -364,6 +396,10 @@ def oracle_sample_rate(name, w, seconds, seed=21):
     if cfg["kind"] == "norm":
         _, row_bytes, _ = workload_stats(name, dict(rows=1, hidden=host["hidden"]))
         work = row_bytes * int(wr.sum())  # algorithmic bytes of the sampled rows
+    elif cfg["kind"] == "moe":
+        ts = host["token_selected"][pos]
+        pairs = int((np.asarray(ts) >= 0).sum())
+        work = 2.0 * pairs * 3 * host["inter"] * host["hidden"]
     else:
         work = 2.0 * host["k"] * int(wr.sum())
     return work / dt, count, dt, oracle.num_threads(), pos, ref, wr
@@ -520,12 +556,16 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1)
     e2e_value = throughput_tflops(world, flops_step, e2e_steps, max_over_ranks(e2e_ms, dev), div)
     value = throughput_tflops(world, flops_step, args.steps, region_ms, div)
-    launches = args.steps * calls_per_step
+    # our kernels per call: the MoE layer launches route, quantise, fc1, SwiGLU,
+    # fc2 and combine
+    launches = args.steps * calls_per_step * (6 if kind == "moe" else 1)
     avg_launch_s = region_ms * 1e-3 / launches
     peaks, peaks_src = load_peaks()
     kernel_name = {"dense": "gemm_kernel<dense>", "grouped": "gemm_kernel<grouped>",
                    "masked": "gemm_kernel<masked>",
-                   "norm": "fused_add_rmsnorm_quant_kernel"}[kind]
+                   "norm": "fused_add_rmsnorm_quant_kernel",
+                   "moe": "moe layer (route, quantise, 2 x gemm_kernel<grouped>, SwiGLU, "
+                          "combine)"}[kind]
     if bound == "tensor":
         achieved = flops_call / avg_launch_s / 1e12
         peak = fp8_peak_tflops(peaks)
@@ -554,13 +594,15 @@ def run_ours(args):
                                                                     args.cpu_seconds)
         cpu_baseline = {"value": rate / div, "unit": unit_v, "cores": threads, "kind": "oracle",
                         "sample": "%d seeded %s of one %s call (%.1f s)"
-                                  % (count, "rows" if kind == "norm" else "output elements",
-                                     args.workload, dt)}
+                                  % (count, {"norm": "rows", "moe": "tokens"}.get(
+                                      kind, "output elements"), args.workload, dt)}
         # spot check of the benchmarked kernel's output at the oracle's positions
         # (set 0 was last written by the end-to-end loop from the same inputs)
         torch.cuda.synchronize(dev)
         if kind == "norm":
             spot = norm_spot_check(w0, pos, ref)
+        elif kind == "moe":
+            spot = moe_spot_check(w0, pos, ref)
         else:
             ref = np.asarray(ref)
             rms = float(np.sqrt(np.mean(ref[wr] ** 2)))
@@ -585,6 +627,8 @@ def run_ours(args):
             "ms_per_step": region_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "f32" if kind == "norm" else "fp8_e4m3",
+            **({"e2e_note": "expert weights resident; each step copies the input and the "
+                            "routing in and the output back"} if kind == "moe" else {}),
             "data": "synthetic",
             "config": config_block(args.workload, sets, calls_per_step, world),
             "roofline": roofline, "cpu_baseline": cpu_baseline,
@@ -601,8 +645,27 @@ def run_ours(args):
 
 # tensors copied in and out by the end-to-end leg (default: everything but
 # `out` in, `out` back)
-INPUT_KEYS = {"norm": ("input", "residual", "weight")}
-OUTPUT_KEYS = {"norm": ("out", "block_scale", "normed_out", "residual")}
+INPUT_KEYS = {"norm": ("input", "residual", "weight"),
+              # the expert weights stay resident, as in serving
+              "moe": ("input", "token_selected")}
+OUTPUT_KEYS = {"norm": ("out", "block_scale", "normed_out", "residual"), "moe": ("out",)}
+
+
+def moe_spot_check(w, tokens, ref):
+    """The MoE layer's output on the oracle's tokens, within the layer's
+    tolerance (|gpu - ref| <= 2e-2 |ref| + 2e-2 rms(ref)) and bit-equal for at
+    least 99% of the elements."""
+    import numpy as np
+    import torch
+    idx = torch.as_tensor(tokens, device=w["out"].device)
+    got = w["out"][idx].float().cpu().double().numpy()
+    r = (np.asarray(ref).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    rms = float(np.sqrt(np.mean(r ** 2)))
+    ok = bool(np.all(np.abs(got - r) <= 2e-2 * np.abs(r) + 2e-2 * rms))
+    got_bits = w["out"][idx].cpu().view(torch.int16).numpy().view(np.uint16)
+    exact = float(np.mean(got_bits == np.asarray(ref)))
+    return {"elements": int(r.size), "tokens": int(len(tokens)), "bit_equal": exact,
+            "within_tolerance": ok and exact >= 0.99}
 
 
 def norm_spot_check(w, rows, ref):

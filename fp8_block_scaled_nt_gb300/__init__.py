@@ -29,6 +29,7 @@ __all__ = [
     "fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
     "gemm_fp8_nt_groupwise", "group_deepgemm_fp8_nt_groupwise",
     "batch_deepgemm_fp8_nt_groupwise", "fused_add_rmsnorm_fp8_block_quant",
+    "fused_moe_deepseek_fp8_block_scale", "moe_workspace_size",
     "OK", "ERR_INVALID_ARGUMENT", "ERR_UNSUPPORTED", "ERR_ARCH", "ERR_CUDA", "ERR_TIMEOUT",
     "DEVICE_TIMEOUT", "DEVICE_BAD_M_INDICES", "DEVICE_MASKED_M_CLAMPED",
 ]
@@ -68,8 +69,13 @@ def load():
     lib.fp8g_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
     lib.fused_add_rmsnorm_fp8_block_quant.argtypes = [P, P, P, P, P, P, ctypes.c_float, I64,
                                                       I64, P]
+    lib.fused_moe_deepseek_fp8_block_scale_workspace_size.argtypes = [I64, I64, I64, I64, I64]
+    lib.fused_moe_deepseek_fp8_block_scale_workspace_size.restype = ctypes.c_size_t
+    lib.fused_moe_deepseek_fp8_block_scale.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64,
+                                                       I64, P, ctypes.c_size_t, P]
     for f in ("fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
-              "fused_add_rmsnorm_fp8_block_quant", "fp8g_get_device_status"):
+              "fused_add_rmsnorm_fp8_block_quant", "fused_moe_deepseek_fp8_block_scale",
+              "fp8g_get_device_status"):
         getattr(lib, f).restype = ctypes.c_int
     lib.fp8g_last_error.argtypes = []
     lib.fp8g_last_error.restype = ctypes.c_char_p
@@ -273,6 +279,56 @@ def fused_add_rmsnorm_fp8_block_quant(out, block_scale, normed_out, input, resid
         _ptr(out), _ptr(block_scale), _ptr(normed_out), _ptr(input), _ptr(residual),
         _ptr(weight), float(eps), rows, hidden, _stream_handle(stream, dev))
     _raise_on(rc, "fused_add_rmsnorm_fp8_block_quant")
+
+
+def moe_workspace_size(num_tokens, num_experts, top_k, hidden_size, inter_size):
+    """Bytes of device workspace fused_moe_deepseek_fp8_block_scale needs."""
+    return int(load().fused_moe_deepseek_fp8_block_scale_workspace_size(
+        num_tokens, num_experts, top_k, hidden_size, inter_size))
+
+
+def fused_moe_deepseek_fp8_block_scale(input, token_selected, fc1_weights, fc2_weights, out,
+                                       fc1_scales, fc2_scales, workspace=None, stream=None):
+    """DeepSeek FP8 block-scale MoE layer (see include/fp8g.h): out (T, H) BF16 =
+    sum over each token's selected experts of fc2(SwiGLU(fc1(input))).
+
+    ``workspace`` is a uint8 CUDA tensor of at least ``moe_workspace_size(...)``
+    bytes; when omitted one is allocated with torch for this call.
+    """
+    torch = _torch()
+    _need(input.dim() == 2 and input.dtype == torch.bfloat16, "input must be bfloat16 (T, H)")
+    t, hdim = input.shape
+    _need(token_selected.dim() == 2 and token_selected.dtype == torch.int32 and
+          token_selected.shape[0] == t, "token_selected must be int32 (T, top_k)")
+    top_k = token_selected.shape[1]
+    _e4m3(fc1_weights, "fc1_weights"), _e4m3(fc2_weights, "fc2_weights")
+    _need(fc1_weights.dim() == 3 and fc1_weights.shape[2] == hdim,
+          "fc1_weights must be (E, 2 I, H)")
+    e, two_i = fc1_weights.shape[0], fc1_weights.shape[1]
+    inter = two_i // 2
+    _need(two_i % 2 == 0 and tuple(fc2_weights.shape) == (e, hdim, inter),
+          "fc2_weights must be (E, H, I)")
+    _need(fc1_scales.dtype == torch.float32 and
+          tuple(fc1_scales.shape) == (e, two_i // 128, hdim // 128),
+          "fc1_scales must be float32 (E, 2 I / 128, H / 128)")
+    _need(fc2_scales.dtype == torch.float32 and
+          tuple(fc2_scales.shape) == (e, hdim // 128, inter // 128),
+          "fc2_scales must be float32 (E, H / 128, I / 128)")
+    _need(out.dtype == torch.bfloat16 and tuple(out.shape) == (t, hdim),
+          "out must be bfloat16 (T, H)")
+    dev = _cuda_contig((input, token_selected, fc1_weights, fc2_weights, out, fc1_scales,
+                        fc2_scales), ("input", "token_selected", "fc1_weights", "fc2_weights",
+                                      "out", "fc1_scales", "fc2_scales"))
+    need = moe_workspace_size(t, e, top_k, hdim, inter)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _cuda_contig((workspace,), ("workspace",))
+    rc = load().fused_moe_deepseek_fp8_block_scale(
+        _ptr(input), _ptr(token_selected), _ptr(fc1_weights), _ptr(fc2_weights), _ptr(out),
+        _ptr(fc1_scales), _ptr(fc2_scales), t, e, top_k, hdim, inter, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
+    _raise_on(rc, "fused_moe_deepseek_fp8_block_scale")
+    return out
 
 
 # ------------------------------------------------------------- page signatures

@@ -19,6 +19,7 @@
 
 #include "fp8g.h"
 #include "gemm_kernel.cuh"
+#include "moe.cuh"
 #include "norm_quant.cuh"
 
 namespace {
@@ -56,6 +57,7 @@ struct DeviceState {
     unsigned int* status = nullptr;
     bool kernel_ready[kNumKernels] = {};
     bool norm_ready = false;
+    bool moe_ready = false;
     int resident[kNumKernels] = {};  // CTAs (or CTA pairs) of a persistent grid
 };
 
@@ -234,6 +236,149 @@ Params base_params(const float* a_scale, const float* b_scale, void* out, int64_
     return p;
 }
 
+// Contiguous grouped GEMM on validated arguments (m > 0).
+fp8g_status_t grouped_gemm(DeviceState& ds, const void* a, const void* b, const float* a_scale,
+                           const float* b_scale, const int32_t* m_indices, void* out, int64_t m,
+                           int64_t n, int64_t k, int64_t num_groups, cudaStream_t stream) {
+    const int64_t tiles = ((m + 127) / 128) * ((n + 255) / 256);
+    fp8g_status_t s;
+    CUtensorMap map_a, map_b;
+    if ((s = encode_map(&map_a, a, m, k, fp8g::BLOCK_M, "a")) != FP8G_OK) return s;
+    if ((s = encode_map(&map_b, b, num_groups * n, k, fp8g::BLOCK_N, "b")) != FP8G_OK) return s;
+    Params p = base_params(a_scale, b_scale, out, m, n, k);
+    p.num_tiles = static_cast<int>(tiles);
+    p.num_groups = static_cast<int>(num_groups);
+    p.m_indices = m_indices;
+    p.status = ds.status;
+    return launch<fp8g::FORM_GROUPED, __nv_bfloat16, false>(ds, 2, map_a, map_b, p, tiles, stream);
+}
+
+// Launch of a plain kernel with programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+fp8g_status_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                         cudaStream_t stream, Args... args) {
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(block, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    (void)cudaGetLastError();
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return FP8G_OK;
+}
+
+// Workspace of the MoE layer: the regions, each 256-byte aligned.
+struct MoeWorkspace {
+    int64_t rows;  // M
+    size_t m_indices, row_of, a1, a1_scale, h, a2, a2_scale, y, total;
+};
+
+MoeWorkspace moe_workspace(int64_t tokens, int64_t experts, int64_t top_k, int64_t hidden,
+                           int64_t inter) {
+    MoeWorkspace w{};
+    w.rows = fp8g::moe_rows(tokens, top_k, experts);
+    size_t at = 0;
+    auto take = [&](size_t bytes) {
+        const size_t start = at;
+        at += (bytes + 255) / 256 * 256;
+        return start;
+    };
+    const size_t M = static_cast<size_t>(w.rows);
+    w.m_indices = take(4 * M);
+    w.row_of = take(4 * static_cast<size_t>(tokens * top_k));
+    w.a1 = take(M * hidden);
+    w.a1_scale = take(4 * M * (hidden / 128));
+    w.h = take(2 * M * 2 * inter);
+    w.a2 = take(M * inter);
+    w.a2_scale = take(4 * M * (inter / 128));
+    w.y = take(2 * M * hidden);
+    w.total = at;
+    return w;
+}
+
+fp8g_status_t check_moe_shape(int64_t tokens, int64_t experts, int64_t top_k, int64_t hidden,
+                              int64_t inter) {
+    if (tokens < 0) return fail(FP8G_ERR_INVALID_ARGUMENT, "num_tokens = %lld < 0", (long long)tokens);
+    if (experts <= 0 || experts > fp8g::MOE_MAX_EXPERTS)
+        return fail(FP8G_ERR_INVALID_ARGUMENT, "num_experts = %lld must be in [1, %d]",
+                    (long long)experts, fp8g::MOE_MAX_EXPERTS);
+    if (top_k <= 0 || top_k > experts)
+        return fail(FP8G_ERR_INVALID_ARGUMENT, "top_k = %lld must be in [1, num_experts]",
+                    (long long)top_k);
+    if (hidden <= 0 || hidden % 128)
+        return fail(FP8G_ERR_INVALID_ARGUMENT,
+                    "hidden_size = %lld must be a positive multiple of 128", (long long)hidden);
+    if (inter <= 0 || inter % 128)
+        return fail(FP8G_ERR_INVALID_ARGUMENT,
+                    "inter_size = %lld must be a positive multiple of 128", (long long)inter);
+    const int64_t rows = fp8g::moe_rows(tokens, top_k, experts);
+    if (tokens * top_k > kMaxDim || rows > kMaxDim || experts * 2 * inter > kMaxDim ||
+        experts * hidden > kMaxDim || rows * 2 * inter > (int64_t(1) << 40))
+        return fail(FP8G_ERR_UNSUPPORTED, "MoE problem too large");
+    return FP8G_OK;
+}
+
+// The MoE layer on validated arguments and a workspace of at least
+// moe_workspace(...).total bytes.
+fp8g_status_t moe_run(DeviceState& ds, const void* input, const int32_t* token_selected,
+                      const void* fc1_weights, const void* fc2_weights, void* out,
+                      const float* fc1_scales, const float* fc2_scales, int64_t tokens,
+                      int64_t experts, int64_t top_k, int64_t hidden, int64_t inter,
+                      uint8_t* ws, cudaStream_t stream) {
+    const MoeWorkspace w = moe_workspace(tokens, experts, top_k, hidden, inter);
+    int32_t* m_indices = reinterpret_cast<int32_t*>(ws + w.m_indices);
+    int32_t* row_of = reinterpret_cast<int32_t*>(ws + w.row_of);
+    uint8_t* a1 = ws + w.a1;
+    float* a1_scale = reinterpret_cast<float*>(ws + w.a1_scale);
+    uint16_t* h = reinterpret_cast<uint16_t*>(ws + w.h);
+    uint8_t* a2 = ws + w.a2;
+    float* a2_scale = reinterpret_cast<float*>(ws + w.a2_scale);
+    uint16_t* y = reinterpret_cast<uint16_t*>(ws + w.y);
+    fp8g_status_t s;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!ds.moe_ready) {
+            cudaError_t e = cudaFuncSetAttribute(fp8g::moe_route_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 3 * 4 * fp8g::MOE_MAX_EXPERTS);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+            ds.moe_ready = true;
+        }
+    }
+    if ((s = launch_pdl(fp8g::moe_route_kernel, 1, fp8g::MOE_ROUTE_THREADS,
+                        static_cast<size_t>(12 * experts), stream, token_selected,
+                        static_cast<int>(tokens * top_k), static_cast<int>(experts),
+                        static_cast<int>(w.rows), m_indices, row_of, ds.status)) != FP8G_OK)
+        return s;
+    if ((s = launch_pdl(fp8g::moe_quant_gather_kernel, static_cast<unsigned>(tokens),
+                        fp8g::MOE_ROW_THREADS, 0, stream, static_cast<const uint16_t*>(input),
+                        static_cast<const int32_t*>(row_of), static_cast<int>(top_k),
+                        static_cast<int>(hidden), a1, a1_scale)) != FP8G_OK)
+        return s;
+    if ((s = grouped_gemm(ds, a1, fc1_weights, a1_scale, fc1_scales, m_indices, h, w.rows,
+                          2 * inter, hidden, experts, stream)) != FP8G_OK)
+        return s;
+    if ((s = launch_pdl(fp8g::moe_swiglu_quant_kernel, static_cast<unsigned>(w.rows),
+                        fp8g::MOE_ROW_THREADS, 0, stream, static_cast<const uint16_t*>(h),
+                        static_cast<const int32_t*>(m_indices), static_cast<int>(inter), a2,
+                        a2_scale)) != FP8G_OK)
+        return s;
+    if ((s = grouped_gemm(ds, a2, fc2_weights, a2_scale, fc2_scales, m_indices, y, w.rows,
+                          hidden, inter, experts, stream)) != FP8G_OK)
+        return s;
+    return launch_pdl(fp8g::moe_combine_kernel, static_cast<unsigned>(tokens),
+                      fp8g::MOE_ROW_THREADS, 0, stream, static_cast<const uint16_t*>(y),
+                      static_cast<const int32_t*>(row_of), static_cast<int>(top_k),
+                      static_cast<int>(hidden), static_cast<uint16_t*>(out));
+}
+
 }  // namespace
 
 extern "C" {
@@ -341,16 +486,8 @@ fp8g_status_t fp8_group_gemm_contiguous(const void* a, const void* b, const floa
         if (tiles > kMaxDim) return fail(FP8G_ERR_UNSUPPORTED, "problem has too many tiles");
         DeviceState* ds = nullptr;
         if ((s = device_state(&ds)) != FP8G_OK) return s;
-        CUtensorMap map_a, map_b;
-        if ((s = encode_map(&map_a, a, m, k, fp8g::BLOCK_M, "a")) != FP8G_OK) return s;
-        if ((s = encode_map(&map_b, b, num_groups * n, k, fp8g::BLOCK_N, "b")) != FP8G_OK)
-            return s;
-        Params p = base_params(a_scale, b_scale, out, m, n, k);
-        p.num_tiles = static_cast<int>(tiles);
-        p.num_groups = static_cast<int>(num_groups);
-        p.m_indices = m_indices;
-        p.status = ds->status;
-        return launch<fp8g::FORM_GROUPED, __nv_bfloat16, false>(*ds, 2, map_a, map_b, p, tiles, stream);
+        return grouped_gemm(*ds, a, b, a_scale, b_scale, m_indices, out, m, n, k, num_groups,
+                            stream);
     } catch (...) {
         return fail(FP8G_ERR_CUDA, "unexpected exception");
     }
@@ -457,6 +594,53 @@ fp8g_status_t fused_add_rmsnorm_fp8_block_quant(void* out, float* block_scale, v
         if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
         t_last_error.clear();
         return FP8G_OK;
+    } catch (...) {
+        return fail(FP8G_ERR_CUDA, "unexpected exception");
+    }
+}
+
+size_t fused_moe_deepseek_fp8_block_scale_workspace_size(int64_t num_tokens, int64_t num_experts,
+                                                         int64_t top_k, int64_t hidden_size,
+                                                         int64_t inter_size) {
+    if (check_moe_shape(num_tokens, num_experts, top_k, hidden_size, inter_size) != FP8G_OK)
+        return 0;
+    return moe_workspace(num_tokens, num_experts, top_k, hidden_size, inter_size).total;
+}
+
+fp8g_status_t fused_moe_deepseek_fp8_block_scale(
+    const void* input, const int32_t* token_selected, const void* fc1_weights,
+    const void* fc2_weights, void* out, const float* fc1_scales, const float* fc2_scales,
+    int64_t num_tokens, int64_t num_experts, int64_t top_k, int64_t hidden_size,
+    int64_t inter_size, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    try {
+        fp8g_status_t s = check_moe_shape(num_tokens, num_experts, top_k, hidden_size,
+                                          inter_size);
+        if (s != FP8G_OK) return s;
+        if (num_tokens == 0) {
+            t_last_error.clear();
+            return FP8G_OK;
+        }
+        if (!input || !token_selected || !fc1_weights || !fc2_weights || !out || !fc1_scales ||
+            !fc2_scales || !workspace)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "null pointer argument");
+        if (!aligned(input, 16) || !aligned(fc1_weights, 16) || !aligned(fc2_weights, 16) ||
+            !aligned(out, 16) || !aligned(workspace, 256) || !aligned(token_selected, 4) ||
+            !aligned(fc1_scales, 4) || !aligned(fc2_scales, 4))
+            return fail(FP8G_ERR_INVALID_ARGUMENT,
+                        "input, weights and out must be 16-byte aligned, workspace 256-byte "
+                        "aligned, token_selected and scales 4-byte aligned");
+        const size_t need =
+            moe_workspace(num_tokens, num_experts, top_k, hidden_size, inter_size).total;
+        if (workspace_bytes < need)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "workspace of %zu bytes, %zu needed",
+                        workspace_bytes, need);
+        DeviceState* ds = nullptr;
+        if ((s = device_state(&ds)) != FP8G_OK) return s;
+        s = moe_run(*ds, input, token_selected, fc1_weights, fc2_weights, out, fc1_scales,
+                    fc2_scales, num_tokens, num_experts, top_k, hidden_size, inter_size,
+                    static_cast<uint8_t*>(workspace), stream);
+        if (s == FP8G_OK) t_last_error.clear();
+        return s;
     } catch (...) {
         return fail(FP8G_ERR_CUDA, "unexpected exception");
     }

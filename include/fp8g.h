@@ -40,6 +40,7 @@
 #ifndef FP8G_H
 #define FP8G_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #include <cuda_runtime_api.h>
@@ -179,6 +180,47 @@ fp8g_status_t fused_add_rmsnorm_fp8_block_quant(void* out, float* block_scale, v
                                                 const void* input, void* residual,
                                                 const void* weight, float eps, int64_t rows,
                                                 int64_t hidden, cudaStream_t stream);
+
+/*
+ * DeepSeek FP8 block-scale MoE layer ("flashinfer-rs" page, section "API
+ * Example: Fused MoE FP8 (cudarc)", fused_moe_cudarc_deepseek_fp8_block_scale),
+ * built on fp8_group_gemm_contiguous.  With T = num_tokens, K = top_k,
+ * E = num_experts, H = hidden_size, I = inter_size, for every token t:
+ *
+ *   (xq, xs) = 1x128 E4M3 quantisation of input[t]   (scale = amax / 448, as in
+ *                                                     fused_add_rmsnorm_fp8_block_quant)
+ *   for each slot s with e = token_selected[t, s] != -1:
+ *     h   = BF16(fc1_e(xq, xs))     rows [0, I) of h are the gate, [I, 2 I) the up part
+ *     act = silu(h[0:I]) * h[I:2I]  (FP32), then its 1x128 quantisation
+ *     y   = BF16(fc2_e(act))
+ *   out[t] = BF16(sum of y over the token's slots)   (no routing weights: the
+ *                                                     page's signature has none)
+ *
+ * where fc(x)_j = sum_kb blocksum * x_scale[kb] * w_scale[j/128][kb] as in the GEMMs.
+ *
+ *   input           (T, H) BF16.
+ *   token_selected  (T, K) int32 expert ids in [0, E), -1 for an empty slot.  Any
+ *                   other value is skipped and raises FP8G_DEVICE_BAD_M_INDICES.
+ *   fc1_weights     (E, 2 I, H) E4M3;  fc1_scales (E, 2 I / 128, H / 128) FP32.
+ *   fc2_weights     (E, H, I) E4M3;    fc2_scales (E, H / 128, I / 128) FP32.
+ *   out             (T, H) BF16; every element is written (zeros for a token
+ *                   without a valid slot).
+ *   workspace       caller-owned device scratch of at least
+ *                   fused_moe_deepseek_fp8_block_scale_workspace_size(...) bytes,
+ *                   256-byte aligned; its contents on entry do not matter.  Two
+ *                   calls must not share a workspace while both may be running.
+ *   H and I must be positive multiples of 128, 1 <= K <= E <= 4096, T >= 0 (0
+ *   launches nothing).  input, weights and out 16-byte aligned, token_selected
+ *   and scales 4-byte aligned.
+ */
+size_t fused_moe_deepseek_fp8_block_scale_workspace_size(int64_t num_tokens, int64_t num_experts,
+                                                         int64_t top_k, int64_t hidden_size,
+                                                         int64_t inter_size);
+fp8g_status_t fused_moe_deepseek_fp8_block_scale(
+    const void* input, const int32_t* token_selected, const void* fc1_weights,
+    const void* fc2_weights, void* out, const float* fc1_scales, const float* fc2_scales,
+    int64_t num_tokens, int64_t num_experts, int64_t top_k, int64_t hidden_size,
+    int64_t inter_size, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Message of the last failed call on this thread ("" if none); valid until the
  * thread's next call into the library. */

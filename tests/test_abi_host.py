@@ -136,6 +136,38 @@ def test_norm_quant_empty_is_ok_without_device(lib):
     assert _norm(lib.load(), rows=0, out=0, inp=0) == 0
 
 
+def _moe(h, inp=16, ts=16, w1=16, w2=16, out=16, s1=16, s2=16, t=8, e=4, k=2, hd=256, i=128,
+         ws=256, wsb=1 << 30):
+    return h.fused_moe_deepseek_fp8_block_scale(inp, ts, w1, w2, out, s1, s2, t, e, k, hd, i,
+                                                ws, wsb, None)
+
+
+@pytest.mark.parametrize("kwargs,status,msg", [
+    (dict(hd=200), 1, "hidden_size"),
+    (dict(i=100), 1, "inter_size"),
+    (dict(k=5), 1, "top_k"),
+    (dict(e=0), 1, "num_experts"),
+    (dict(e=5000, k=2), 1, "num_experts"),
+    (dict(t=-1), 1, "num_tokens"),
+    (dict(ws=0), 1, "null"),
+    (dict(ws=272), 1, "256-byte"),
+    (dict(wsb=1000), 1, "workspace of 1000 bytes"),
+])
+def test_moe_host_validation(lib, kwargs, status, msg):
+    h = lib.load()
+    assert _moe(h, **kwargs) == status
+    assert msg in lib.last_error()
+
+
+def test_moe_workspace_size_and_empty_call(lib):
+    # rows bound: round_up(T*K + 127*E, 128); regions 256-byte aligned
+    size = lib.moe_workspace_size(8, 4, 2, 256, 128)
+    rows = (8 * 2 + 127 * 4 + 127) // 128 * 128
+    assert size >= rows * (256 + 2 * 256 + 128 + 2 * 256) and size % 256 == 0
+    assert lib.moe_workspace_size(8, 4, 2, 200, 128) == 0  # bad shape
+    assert _moe(lib.load(), t=0, inp=0, out=0, ws=0, wsb=0) == 0
+
+
 def test_valid_call_without_a_device_reports_cuda_error(lib):
     import torch
     if torch.cuda.is_available():

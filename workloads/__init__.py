@@ -46,6 +46,12 @@ CONFIGS = {
     # the producer of the GEMM's activations: 4096 tokens of hidden size 7168
     # (the k of the MoE workloads above)
     "norm_quant_4096x7168": dict(kind="norm", rows=4096, hidden=7168, eps=1e-6, seed=1006),
+    # the DeepSeek FP8 block-scale MoE layer around the grouped GEMM: fc1 is the
+    # grouped workload above (n = 2 * inter = 4096, k = hidden = 7168), fc2 has
+    # n = 7168, k = 2048
+    "moe_4096tok_top8_e64_h7168_i2048": dict(kind="moe", tokens=4096, top_k=8, num_experts=64,
+                                             hidden=7168, inter=2048, scale_exp=(-7.0, -5.0),
+                                             seed=1008),
 }
 
 
@@ -181,6 +187,29 @@ def norm(rows, hidden, seed, eps=1e-6, device="cpu", **_):
                 hidden=hidden, eps=eps)
 
 
+def moe(tokens, top_k, num_experts, hidden, inter, seed, scale_exp=(-7.0, -5.0), device="cpu",
+        **_):
+    """Operands of the DeepSeek FP8 block-scale MoE layer: BF16 input ~ N(0, 1);
+    token_selected (tokens, top_k) int32, each token's distinct experts drawn
+    uniformly without replacement; E4M3 fc1 (E, 2 inter, hidden) and fc2 (E,
+    hidden, inter) ~ N(0, 1); 128 x 128 block scales 2**U(lo, hi)."""
+    cpu_gen = generator(seed, "cpu")
+    w = torch.ones((tokens, num_experts), dtype=torch.float32)
+    ts = torch.multinomial(w, top_k, replacement=False, generator=cpu_gen).to(torch.int32)
+    gen = generator(seed + 7919, device)
+    x = torch.empty((tokens, hidden), dtype=torch.float32, device=device)
+    x.normal_(0.0, 1.0, generator=gen)
+    fc1 = _draw((num_experts, 2 * inter, hidden), "normal", gen, device)
+    fc2 = _draw((num_experts, hidden, inter), "normal", gen, device)
+    s1 = log_uniform((num_experts, 2 * inter // KBLOCK, hidden // KBLOCK), scale_exp[0],
+                     scale_exp[1], gen, device)
+    s2 = log_uniform((num_experts, hidden // KBLOCK, inter // KBLOCK), scale_exp[0],
+                     scale_exp[1], gen, device)
+    return dict(input=x.to(torch.bfloat16), token_selected=ts.to(device), fc1=fc1, fc2=fc2,
+                fc1_scale=s1, fc2_scale=s2, tokens=tokens, top_k=top_k,
+                num_experts=num_experts, hidden=hidden, inter=inter)
+
+
 def make(name, device="cpu", **overrides):
     """Operands of one of the named workloads."""
     cfg = dict(CONFIGS[name])
@@ -194,6 +223,8 @@ def make(name, device="cpu", **overrides):
         return masked(device=device, **cfg)
     if kind == "norm":
         return norm(device=device, **cfg)
+    if kind == "moe":
+        return moe(device=device, **cfg)
     raise ValueError(kind)
 
 
