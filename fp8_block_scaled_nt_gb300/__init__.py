@@ -30,6 +30,7 @@ __all__ = [
     "gemm_fp8_nt_groupwise", "group_deepgemm_fp8_nt_groupwise",
     "batch_deepgemm_fp8_nt_groupwise", "fused_add_rmsnorm_fp8_block_quant",
     "fused_moe_deepseek_fp8_block_scale", "moe_workspace_size",
+    "fused_moe_deepseek_fp8_block_scale_noalloc", "MOE_STATIC_SCRATCH_BYTES",
     "OK", "ERR_INVALID_ARGUMENT", "ERR_UNSUPPORTED", "ERR_ARCH", "ERR_CUDA", "ERR_TIMEOUT",
     "DEVICE_TIMEOUT", "DEVICE_BAD_M_INDICES", "DEVICE_MASKED_M_CLAMPED",
 ]
@@ -42,6 +43,7 @@ STATUS_NAMES = {0: "FP8G_OK", 1: "FP8G_ERR_INVALID_ARGUMENT", 2: "FP8G_ERR_UNSUP
 SCALE_K_MAJOR, SCALE_MN_MAJOR = 0, 1
 OUT_BF16, OUT_F16, OUT_E4M3 = 0, 1, 2
 DEVICE_TIMEOUT, DEVICE_BAD_M_INDICES, DEVICE_MASKED_M_CLAMPED = 0x1, 0x2, 0x4
+MOE_STATIC_SCRATCH_BYTES = 64 << 20  # FP8G_MOE_STATIC_SCRATCH_BYTES
 
 
 class Fp8gError(RuntimeError):
@@ -73,9 +75,11 @@ def load():
     lib.fused_moe_deepseek_fp8_block_scale_workspace_size.restype = ctypes.c_size_t
     lib.fused_moe_deepseek_fp8_block_scale.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64,
                                                        I64, P, ctypes.c_size_t, P]
+    lib.fused_moe_deepseek_fp8_block_scale_noalloc.argtypes = [P, P, P, P, P, P, P, I64, I64,
+                                                               I64, I64, I64, P]
     for f in ("fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
               "fused_add_rmsnorm_fp8_block_quant", "fused_moe_deepseek_fp8_block_scale",
-              "fp8g_get_device_status"):
+              "fused_moe_deepseek_fp8_block_scale_noalloc", "fp8g_get_device_status"):
         getattr(lib, f).restype = ctypes.c_int
     lib.fp8g_last_error.argtypes = []
     lib.fp8g_last_error.restype = ctypes.c_char_p
@@ -328,6 +332,28 @@ def fused_moe_deepseek_fp8_block_scale(input, token_selected, fc1_weights, fc2_w
         _ptr(fc1_scales), _ptr(fc2_scales), t, e, top_k, hdim, inter, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
     _raise_on(rc, "fused_moe_deepseek_fp8_block_scale")
+    return out
+
+
+def fused_moe_deepseek_fp8_block_scale_noalloc(input, token_selected, fc1_weights, fc2_weights,
+                                               out, fc1_scales, fc2_scales, stream=None):
+    """The MoE layer with its scratch in the library's fixed per-device array
+    (MOE_STATIC_SCRATCH_BYTES); nothing is allocated.  Calls that can overlap on
+    one device race on that scratch."""
+    torch = _torch()
+    t, hdim = input.shape
+    top_k = token_selected.shape[1]
+    e, two_i = fc1_weights.shape[0], fc1_weights.shape[1]
+    _need(input.dtype == torch.bfloat16 and out.dtype == torch.bfloat16 and
+          token_selected.dtype == torch.int32, "input/out bfloat16, token_selected int32")
+    dev = _cuda_contig((input, token_selected, fc1_weights, fc2_weights, out, fc1_scales,
+                        fc2_scales), ("input", "token_selected", "fc1_weights", "fc2_weights",
+                                      "out", "fc1_scales", "fc2_scales"))
+    rc = load().fused_moe_deepseek_fp8_block_scale_noalloc(
+        _ptr(input), _ptr(token_selected), _ptr(fc1_weights), _ptr(fc2_weights), _ptr(out),
+        _ptr(fc1_scales), _ptr(fc2_scales), t, e, top_k, hdim, two_i // 2,
+        _stream_handle(stream, dev))
+    _raise_on(rc, "fused_moe_deepseek_fp8_block_scale_noalloc")
     return out
 
 

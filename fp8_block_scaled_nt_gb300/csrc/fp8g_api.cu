@@ -28,6 +28,9 @@ using fp8g::Params;
 
 __device__ unsigned int g_device_status;  // OR of FP8G_DEVICE_* bits, per device
 
+// Fixed scratch of the MoE layer's allocation-free entry point, one per device.
+static __device__ __align__(256) uint8_t g_moe_static_scratch[FP8G_MOE_STATIC_SCRATCH_BYTES];
+
 thread_local std::string t_last_error;
 
 fp8g_status_t fail(fp8g_status_t s, const char* fmt, ...) {
@@ -58,6 +61,7 @@ struct DeviceState {
     bool kernel_ready[kNumKernels] = {};
     bool norm_ready = false;
     bool moe_ready = false;
+    uint8_t* moe_static_scratch = nullptr;  // address of g_moe_static_scratch on this device
     int resident[kNumKernels] = {};  // CTAs (or CTA pairs) of a persistent grid
 };
 
@@ -639,6 +643,58 @@ fp8g_status_t fused_moe_deepseek_fp8_block_scale(
         s = moe_run(*ds, input, token_selected, fc1_weights, fc2_weights, out, fc1_scales,
                     fc2_scales, num_tokens, num_experts, top_k, hidden_size, inter_size,
                     static_cast<uint8_t*>(workspace), stream);
+        if (s == FP8G_OK) t_last_error.clear();
+        return s;
+    } catch (...) {
+        return fail(FP8G_ERR_CUDA, "unexpected exception");
+    }
+}
+
+fp8g_status_t fused_moe_deepseek_fp8_block_scale_noalloc(
+    const void* input, const int32_t* token_selected, const void* fc1_weights,
+    const void* fc2_weights, void* out, const float* fc1_scales, const float* fc2_scales,
+    int64_t num_tokens, int64_t num_experts, int64_t top_k, int64_t hidden_size,
+    int64_t inter_size, cudaStream_t stream) {
+    try {
+        fp8g_status_t s = check_moe_shape(num_tokens, num_experts, top_k, hidden_size,
+                                          inter_size);
+        if (s != FP8G_OK) return s;
+        if (num_tokens == 0) {
+            t_last_error.clear();
+            return FP8G_OK;
+        }
+        if (!input || !token_selected || !fc1_weights || !fc2_weights || !out || !fc1_scales ||
+            !fc2_scales)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "null pointer argument");
+        if (!aligned(input, 16) || !aligned(fc1_weights, 16) || !aligned(fc2_weights, 16) ||
+            !aligned(out, 16) || !aligned(token_selected, 4) || !aligned(fc1_scales, 4) ||
+            !aligned(fc2_scales, 4))
+            return fail(FP8G_ERR_INVALID_ARGUMENT,
+                        "input, weights and out must be 16-byte aligned, token_selected and "
+                        "scales 4-byte aligned");
+        const size_t need =
+            moe_workspace(num_tokens, num_experts, top_k, hidden_size, inter_size).total;
+        if (need > static_cast<size_t>(FP8G_MOE_STATIC_SCRATCH_BYTES))
+            return fail(FP8G_ERR_UNSUPPORTED,
+                        "this problem needs %zu bytes of scratch; the static scratch holds %zu "
+                        "(use fused_moe_deepseek_fp8_block_scale with a workspace)",
+                        need, static_cast<size_t>(FP8G_MOE_STATIC_SCRATCH_BYTES));
+        DeviceState* ds = nullptr;
+        if ((s = device_state(&ds)) != FP8G_OK) return s;
+        uint8_t* scratch = nullptr;
+        {
+            std::lock_guard<std::mutex> lock(g_mutex);
+            if (!ds->moe_static_scratch) {
+                void* addr = nullptr;
+                cudaError_t e = cudaGetSymbolAddress(&addr, g_moe_static_scratch);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+                ds->moe_static_scratch = static_cast<uint8_t*>(addr);
+            }
+            scratch = ds->moe_static_scratch;
+        }
+        s = moe_run(*ds, input, token_selected, fc1_weights, fc2_weights, out, fc1_scales,
+                    fc2_scales, num_tokens, num_experts, top_k, hidden_size, inter_size, scratch,
+                    stream);
         if (s == FP8G_OK) t_last_error.clear();
         return s;
     } catch (...) {

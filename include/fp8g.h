@@ -222,6 +222,30 @@ fp8g_status_t fused_moe_deepseek_fp8_block_scale(
     int64_t num_tokens, int64_t num_experts, int64_t top_k, int64_t hidden_size,
     int64_t inter_size, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * The MoE layer above without a caller workspace: the same computation, with its
+ * scratch in a fixed array of FP8G_MOE_STATIC_SCRATCH_BYTES per device that the
+ * library defines statically (no allocation at call time, by the library or
+ * anyone else).  The pages have no counterpart of this call; it serves callers
+ * that cannot provide device memory.
+ *
+ *   - Problems whose scratch (fused_moe_deepseek_fp8_block_scale_workspace_size)
+ *     exceeds FP8G_MOE_STATIC_SCRATCH_BYTES return FP8G_ERR_UNSUPPORTED with a
+ *     message giving both sizes; nothing is launched.
+ *   - Nothing in the scratch has to start at zero: the routing step writes every
+ *     entry of the layout it reads back, and every other region is written
+ *     before it is read within the same call.
+ *   - There is one scratch per device: calls that may run at the same time on
+ *     one device (different streams, or host threads) race on it and corrupt
+ *     each other's results.  Calls in one stream are ordered and safe.
+ */
+#define FP8G_MOE_STATIC_SCRATCH_BYTES (64u << 20) /* 64 MiB */
+fp8g_status_t fused_moe_deepseek_fp8_block_scale_noalloc(
+    const void* input, const int32_t* token_selected, const void* fc1_weights,
+    const void* fc2_weights, void* out, const float* fc1_scales, const float* fc2_scales,
+    int64_t num_tokens, int64_t num_experts, int64_t top_k, int64_t hidden_size,
+    int64_t inter_size, cudaStream_t stream);
+
 /* Message of the last failed call on this thread ("" if none); valid until the
  * thread's next call into the library. */
 const char* fp8g_last_error(void);

@@ -168,6 +168,15 @@ def test_moe_workspace_size_and_empty_call(lib):
     assert _moe(lib.load(), t=0, inp=0, out=0, ws=0, wsb=0) == 0
 
 
+def test_moe_noalloc_rejects_oversize_on_the_host(lib):
+    h = lib.load()
+    # 8192 tokens x top-2, hidden 1024, inter 512: far beyond the 64 MiB scratch
+    assert lib.moe_workspace_size(8192, 4, 2, 1024, 512) > lib.MOE_STATIC_SCRATCH_BYTES
+    rc = h.fused_moe_deepseek_fp8_block_scale_noalloc(16, 16, 16, 16, 16, 16, 16, 8192, 4, 2,
+                                                      1024, 512, None)
+    assert rc == 2 and "static scratch" in lib.last_error()
+
+
 def test_valid_call_without_a_device_reports_cuda_error(lib):
     import torch
     if torch.cuda.is_available():
