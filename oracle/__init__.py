@@ -20,6 +20,8 @@ from . import build as _build
 
 OUT_BF16 = 0
 OUT_F16 = 1
+FP8_E4M3 = 0
+FP8_E5M2 = 1
 SCALE_K_MAJOR = 0
 SCALE_MN_MAJOR = 1
 
@@ -56,7 +58,11 @@ def _load():
         lib.oracle_quant_1x128.restype = None
         lib.oracle_moe_deepseek_fp8_block_scale.argtypes = [P, P, P, P, P, P, I64, I64, I64,
                                                             I64, I64, P]
+        lib.oracle_e5m2_table.argtypes = [P]
+        lib.oracle_e5m2_table.restype = None
+        lib.oracle_bmm_fp8.argtypes = [P, P, I, I, P, I, P, I, I64, I64, I64, I64, I, P, P]
         for f in ("oracle_gemm_nt_groupwise", "oracle_gemm_nt_groupwise_at",
+                  "oracle_bmm_fp8",
                   "oracle_fused_add_rmsnorm_fp8_block_quant",
                   "oracle_moe_deepseek_fp8_block_scale",
                   "oracle_group_gemm_contiguous", "oracle_group_gemm_contiguous_at",
@@ -306,3 +312,34 @@ def moe_deepseek_fp8_block_scale(input_bits, token_selected, w1, w2, s1, s2):
         raise ValueError("moe: token_selected holds an expert id outside [-1, num_experts)")
     _check(rc, "moe_deepseek_fp8_block_scale")
     return out
+
+
+def e5m2_table():
+    """The 256 E5M2 code values (FP64): +-inf at 0x7C/0xFC, NaN at 0x7D-0x7F, 0xFD-0xFF."""
+    out = np.empty(256, np.float64)
+    _load().oracle_e5m2_table(out.ctypes.data)
+    return out
+
+
+def bmm_fp8(a, b, a_scale, b_scale, a_fmt=FP8_E4M3, b_fmt=FP8_E4M3, out_dtype=OUT_BF16):
+    """bmm_fp8 (section GEMM): A (batch, m, k), B (batch, k, n) FP8 codes; each
+    scale a one-element (tensorwise) or channelwise array — a_scale (batch, m, 1),
+    b_scale (batch, 1, n).  Returns (ref_f64, bits_u16), both (batch, m, n)."""
+    a, b = _arr(a, np.uint8), _arr(b, np.uint8)
+    sa, sb = _arr(a_scale, np.float32), _arr(b_scale, np.float32)
+    batch, m, k = a.shape
+    n = b.shape[2]
+    if b.shape[:2] != (batch, k):
+        raise ValueError("B must be (batch, k, n)")
+    a_ch = sa.size != 1
+    b_ch = sb.size != 1
+    if a_ch and sa.shape != (batch, m, 1):
+        raise ValueError("channelwise a_scale must be (batch, m, 1)")
+    if b_ch and sb.shape != (batch, 1, n):
+        raise ValueError("channelwise b_scale must be (batch, 1, n)")
+    ref = np.empty((batch, m, n), np.float64)
+    bits = np.empty((batch, m, n), np.uint16)
+    rc = _load().oracle_bmm_fp8(_p(a), _p(b), int(a_fmt), int(b_fmt), _p(sa), int(a_ch), _p(sb),
+                                int(b_ch), batch, m, n, k, int(out_dtype), _p(ref), _p(bits))
+    _check(rc, "bmm_fp8")
+    return ref, bits

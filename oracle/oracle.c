@@ -645,3 +645,68 @@ int oracle_moe_deepseek_fp8_block_scale(const uint16_t* input, const int32_t* to
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------- bmm_fp8 */
+
+/* E5M2 (float8_e5m2): sign s, exponent field e (bias 15), mantissa field f.
+ * e == 0 is subnormal: f * 2^-2 * 2^(1-15); e == 31 is infinity (f == 0) or
+ * NaN; otherwise (1 + f/4) * 2^(e-15). */
+void oracle_e5m2_table(double out[256])
+{
+    for (int c = 0; c < 256; ++c) {
+        int s = (c >> 7) & 1;
+        int e = (c >> 2) & 31;
+        int f = c & 3;
+        double v;
+        if (e == 31)
+            v = f == 0 ? INFINITY : NAN;
+        else if (e == 0)
+            v = ldexp((double)f, -16);
+        else
+            v = ldexp((double)(4 + f), e - 17);
+        out[c] = s ? -v : v;
+    }
+}
+
+int oracle_bmm_fp8(const uint8_t* a, const uint8_t* b, int a_fmt, int b_fmt,
+                   const float* a_scale, int a_channelwise, const float* b_scale,
+                   int b_channelwise, int64_t batch, int64_t m, int64_t n, int64_t k,
+                   int out_dtype, double* ref, uint16_t* out)
+{
+    if (batch < 0 || m < 0 || n < 0 || k < 0 || (a_fmt != ORACLE_FP8_E4M3 &&
+        a_fmt != ORACLE_FP8_E5M2) || (b_fmt != ORACLE_FP8_E4M3 && b_fmt != ORACLE_FP8_E5M2))
+        return -1;
+    double deca[256], decb[256];
+    if (a_fmt == ORACLE_FP8_E4M3)
+        oracle_e4m3_table(deca);
+    else
+        oracle_e5m2_table(deca);
+    if (b_fmt == ORACLE_FP8_E4M3)
+        oracle_e4m3_table(decb);
+    else
+        oracle_e5m2_table(decb);
+#pragma omp parallel for collapse(2) schedule(dynamic, 16)
+    for (int64_t bb = 0; bb < batch; ++bb)
+        for (int64_t i = 0; i < m; ++i) {
+            const uint8_t* arow = a + (bb * m + i) * k;
+            const double sa = a_channelwise ? (double)a_scale[bb * m + i] : (double)a_scale[0];
+            for (int64_t j = 0; j < n; ++j) {
+                /* column j of B (batch bb) is b[bb][t][j], t = 0 .. k-1 */
+                double acc = 0.0;
+                for (int64_t t = 0; t < k; ++t)
+                    acc += deca[arow[t]] * decb[b[(bb * k + t) * n + j]];
+                const double sb =
+                    b_channelwise ? (double)b_scale[bb * n + j] : (double)b_scale[0];
+                const double x = acc * (sa * sb);
+                const int64_t o = (bb * m + i) * n + j;
+                uint16_t bits;
+                double y = round_one(x, out_dtype, &bits);
+                (void)y;
+                if (ref)
+                    ref[o] = x;
+                if (out)
+                    out[o] = bits;
+            }
+        }
+    return 0;
+}

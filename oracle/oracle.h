@@ -170,6 +170,28 @@ int oracle_moe_deepseek_fp8_block_scale(const uint16_t* input, const int32_t* to
                                         int64_t num_experts, int64_t top_k, int64_t hidden,
                                         int64_t inter, uint16_t* out);
 
+/* FP8 formats of bmm_fp8's operands. */
+#define ORACLE_FP8_E4M3 0
+#define ORACLE_FP8_E5M2 1
+
+/* The 256-entry E5M2 (float8_e5m2) decode table: 1 sign bit, 5 exponent bits
+ * with bias 15, 2 mantissa bits; exponent 11111 is infinity (mantissa 0) or
+ * NaN. */
+void oracle_e5m2_table(double out[256]);
+
+/* bmm_fp8 of the MATE page "FlashInfer Wrapper APIs", section GEMM: for each
+ * batch bb, out[bb] = (A[bb] @ B[bb]) * a_scale * b_scale with A (batch, m, k)
+ * and B (batch, k, n) row-major FP8 codes (E4M3 or E5M2 each, a_fmt / b_fmt),
+ * and FP32 scales that are either one tensorwise value or channelwise: a_scale
+ * (batch, m, 1) per row of A, b_scale (batch, 1, n) per column of B.
+ *   out[bb][i][j] = round( (sum_t A[bb][i][t] * B[bb][t][j]) * (sa * sb) )
+ * summed in FP64, rounded once to BF16/FP16.  ref/out (batch*m*n), either may
+ * be NULL. */
+int oracle_bmm_fp8(const uint8_t* a, const uint8_t* b, int a_fmt, int b_fmt,
+                   const float* a_scale, int a_channelwise, const float* b_scale,
+                   int b_channelwise, int64_t batch, int64_t m, int64_t n, int64_t k,
+                   int out_dtype, double* ref, uint16_t* out);
+
 /* Number of threads the oracle's parallel loops use. */
 int oracle_num_threads(void);
 

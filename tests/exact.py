@@ -172,3 +172,34 @@ def bf16_bits(v):
     import struct
     f = struct.pack(">f", float(v))
     return int.from_bytes(f[:2], "big")
+
+
+def e5m2_value(code):
+    """Exact value of an E5M2 (float8_e5m2) code, None for NaN or infinity."""
+    s, e, f = (code >> 7) & 1, (code >> 2) & 0x1F, code & 3
+    if e == 0x1F:
+        return None
+    if e == 0:
+        v = Fraction(f, 4) * Fraction(1, 2 ** 14)
+    else:
+        v = (1 + Fraction(f, 4)) * Fraction(2) ** (e - 15)
+    return -v if s else v
+
+
+def bmm(a_codes, b_codes, a_fmt, b_fmt, sa, sb, fmt):
+    """bmm_fp8 (MATE page "FlashInfer Wrapper APIs", section GEMM) exactly:
+    out[bb][i][j] = round((sum_t A[bb][i][t] * B[bb][t][j]) * sa * sb) with sa,
+    sb the FP32 scales of row i / column j (or one tensorwise value each)."""
+    dec = {0: e4m3_value, 1: e5m2_value}
+    batch, m, k = a_codes.shape
+    n = b_codes.shape[2]
+    out = np.empty((batch, m, n), dtype=object)
+    for bb in range(batch):
+        for i in range(m):
+            for j in range(n):
+                acc = sum(dec[a_fmt](int(a_codes[bb, i, t])) * dec[b_fmt](int(b_codes[bb, t, j]))
+                          for t in range(k))
+                s_a = Fraction(float(sa.flat[0] if sa.size == 1 else sa[bb, i, 0]))
+                s_b = Fraction(float(sb.flat[0] if sb.size == 1 else sb[bb, 0, j]))
+                out[bb, i, j] = round_exact(acc * s_a * s_b, fmt)
+    return out
