@@ -196,6 +196,9 @@ def workload_stats(name, w):
         # the live experts' weights and scales, the input and the output
         bytes_ = live * (3 * inter * hdim + 4 * (3 * inter // 128) * (hdim // 128)) + 4 * t * hdim
         return flops, bytes_, "tensor"
+    if kind == "bmm":
+        b_, m_, n_, k_ = w["batch"], w["m"], w["n"], w["k"]
+        return 2.0 * b_ * m_ * n_ * k_, b_ * (m_ * k_ + k_ * n_ + 2 * m_ * n_) + 8, "tensor"
     if kind == "norm":
         rows, hidden = w["rows"], w["hidden"]
         # read input, residual; write residual, normed_out (BF16) and the codes
@@ -263,6 +266,10 @@ def make_sets(name, device):
                 w["workspace"] = torch.empty(fp8g.moe_workspace_size(
                     w["tokens"], w["num_experts"], w["top_k"], w["hidden"], w["inter"]),
                     dtype=torch.uint8, device=device)
+            elif cfg["kind"] == "bmm":
+                w = workloads.make(name, device=device, seed=seed)
+                w["out"] = torch.empty((w["batch"], w["m"], w["n"]), dtype=torch.bfloat16,
+                                       device=device)
             elif cfg["kind"] == "norm":
                 w = workloads.make(name, device=device, seed=seed)
                 rows, hidden = w["rows"], w["hidden"]
@@ -306,6 +313,13 @@ def call_args(lib, name, w, stream_handle):
                  p(w["fc1_scale"]), p(w["fc2_scale"]), w["tokens"], w["num_experts"],
                  w["top_k"], w["hidden"], w["inter"], p(w["workspace"]),
                  w["workspace"].numel(), stream_handle))
+    if kind == "bmm":
+        import torch
+        fmt = lambda t: 1 if t.dtype == torch.float8_e5m2 else 0  # noqa: E731
+        return (lib.bmm_fp8,
+                (p(w["A"]), p(w["B"]), fmt(w["A"]), fmt(w["B"]), p(w["A_scale"]), 0,
+                 p(w["B_scale"]), 0, p(w["out"]), 0, w["batch"], w["m"], w["n"], w["k"],
+                 stream_handle))
     if kind == "norm":
         return (lib.fused_add_rmsnorm_fp8_block_quant,
                 (p(w["out"]), p(w["block_scale"]), p(w["normed_out"]), p(w["input"]),
@@ -336,6 +350,15 @@ def oracle_sample_rate(name, w, seconds, seed=21):
 
     def run(count):
         g = np.random.default_rng(seed)
+        if cfg["kind"] == "bmm":
+            import torch
+            r = np.sort(g.choice(host["m"], size=min(count, host["m"]), replace=False))
+            fmt = lambda t: 1 if t.dtype == torch.float8_e5m2 else 0  # noqa: E731
+            t0 = time.perf_counter()
+            ref, _ = oracle.bmm_fp8(host["A"].view(torch.uint8)[:1, torch.as_tensor(r)],
+                                    host["B"].view(torch.uint8)[:1], host["A_scale"].numpy(),
+                                    host["B_scale"].numpy(), fmt(host["A"]), fmt(host["B"]))
+            return time.perf_counter() - t0, r, ref[0], np.ones(r.size, bool)
         if cfg["kind"] == "moe":
             r = np.sort(g.choice(host["tokens"], size=min(count, host["tokens"]), replace=False))
             t0 = time.perf_counter()
@@ -384,6 +407,8 @@ def oracle_sample_rate(name, w, seconds, seed=21):
         count, limit = 4, host["rows"]
     elif cfg["kind"] == "moe":
         count, limit = 1, host["tokens"]
+    elif cfg["kind"] == "bmm":
+        count, limit = 1, host["m"]
     else:
         count, limit = 4096, 50_000_000
     while True:
@@ -396,6 +421,8 @@ def oracle_sample_rate(name, w, seconds, seed=21):
     if cfg["kind"] == "norm":
         _, row_bytes, _ = workload_stats(name, dict(rows=1, hidden=host["hidden"]))
         work = row_bytes * int(wr.sum())  # algorithmic bytes of the sampled rows
+    elif cfg["kind"] == "bmm":
+        work = 2.0 * int(wr.sum()) * host["n"] * host["k"]
     elif cfg["kind"] == "moe":
         ts = host["token_selected"][pos]
         pairs = int((np.asarray(ts) >= 0).sum())
@@ -565,7 +592,7 @@ def run_ours(args):
     peaks, peaks_src = load_peaks()
     kernel_name = {"dense": "gemm_kernel<dense>", "grouped": "gemm_kernel<grouped>",
                    "masked": "gemm_kernel<masked>",
-                   "norm": "fused_add_rmsnorm_quant_kernel",
+                   "norm": "fused_add_rmsnorm_quant_kernel", "bmm": "bmm_kernel",
                    "moe": "moe layer (route, quantise, 2 x gemm_kernel<grouped>, SwiGLU, "
                           "combine)"}[kind]
     if bound == "tensor":
@@ -596,7 +623,8 @@ def run_ours(args):
                                                                     args.cpu_seconds)
         cpu_baseline = {"value": rate / div, "unit": unit_v, "cores": threads, "kind": "oracle",
                         "sample": "%d seeded %s of one %s call (%.1f s)"
-                                  % (count, {"norm": "rows", "moe": "tokens"}.get(
+                                  % (count, {"norm": "rows", "moe": "tokens",
+                                             "bmm": "rows of batch 0"}.get(
                                       kind, "output elements"), args.workload, dt)}
         # spot check of the benchmarked kernel's output at the oracle's positions
         # (set 0 was last written by the end-to-end loop from the same inputs)
@@ -605,6 +633,14 @@ def run_ours(args):
             spot = norm_spot_check(w0, pos, ref)
         elif kind == "moe":
             spot = moe_spot_check(w0, pos, ref)
+        elif kind == "bmm":
+            got = w0["out"][0, torch.as_tensor(pos, device=w0["out"].device)].float().cpu() \
+                .double().numpy()
+            ref = np.asarray(ref)
+            rms = float(np.sqrt(np.mean(ref ** 2)))
+            ok = bool(np.all(np.abs(got - ref) <= 1e-2 * np.abs(ref) + 2e-3 * rms))
+            spot = {"elements": int(ref.size), "rows_of_batch_0": int(len(pos)),
+                    "within_tolerance": ok}
         else:
             ref = np.asarray(ref)
             rms = float(np.sqrt(np.mean(ref[wr] ** 2)))

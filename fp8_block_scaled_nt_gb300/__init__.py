@@ -30,7 +30,7 @@ __all__ = [
     "gemm_fp8_nt_groupwise", "group_deepgemm_fp8_nt_groupwise",
     "batch_deepgemm_fp8_nt_groupwise", "fused_add_rmsnorm_fp8_block_quant",
     "fused_moe_deepseek_fp8_block_scale", "moe_workspace_size",
-    "fused_moe_deepseek_fp8_block_scale_noalloc", "MOE_STATIC_SCRATCH_BYTES",
+    "fused_moe_deepseek_fp8_block_scale_noalloc", "MOE_STATIC_SCRATCH_BYTES", "bmm_fp8",
     "OK", "ERR_INVALID_ARGUMENT", "ERR_UNSUPPORTED", "ERR_ARCH", "ERR_CUDA", "ERR_TIMEOUT",
     "DEVICE_TIMEOUT", "DEVICE_BAD_M_INDICES", "DEVICE_MASKED_M_CLAMPED",
 ]
@@ -69,6 +69,7 @@ def load():
     lib.fp8_group_gemm_contiguous.argtypes = [P, P, P, P, P, P, I64, I64, I64, I64, P]
     lib.fp8_batch_gemm_masked.argtypes = [P, P, P, P, P, I64, P, I64, I64, I64, I64, P]
     lib.fp8g_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), I]
+    lib.bmm_fp8.argtypes = [P, P, I, I, P, I, P, I, P, I, I64, I64, I64, I64, P]
     lib.fused_add_rmsnorm_fp8_block_quant.argtypes = [P, P, P, P, P, P, ctypes.c_float, I64,
                                                       I64, P]
     lib.fused_moe_deepseek_fp8_block_scale_workspace_size.argtypes = [I64, I64, I64, I64, I64]
@@ -78,7 +79,7 @@ def load():
     lib.fused_moe_deepseek_fp8_block_scale_noalloc.argtypes = [P, P, P, P, P, P, P, I64, I64,
                                                                I64, I64, I64, P]
     for f in ("fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
-              "fused_add_rmsnorm_fp8_block_quant", "fused_moe_deepseek_fp8_block_scale",
+              "fused_add_rmsnorm_fp8_block_quant", "fused_moe_deepseek_fp8_block_scale", "bmm_fp8",
               "fused_moe_deepseek_fp8_block_scale_noalloc", "fp8g_get_device_status"):
         getattr(lib, f).restype = ctypes.c_int
     lib.fp8g_last_error.argtypes = []
@@ -354,6 +355,42 @@ def fused_moe_deepseek_fp8_block_scale_noalloc(input, token_selected, fc1_weight
         _ptr(fc1_scales), _ptr(fc2_scales), t, e, top_k, hdim, two_i // 2,
         _stream_handle(stream, dev))
     _raise_on(rc, "fused_moe_deepseek_fp8_block_scale_noalloc")
+    return out
+
+
+def bmm_fp8(A, B, A_scale, B_scale, dtype=None, out=None, backend="auto", stream=None):
+    """The page's ``bmm_fp8``: out (batch, m, n) = A (batch, m, k) @ B (batch, k, n)
+    times the scales.  A and B are ``float8_e4m3fn`` or ``float8_e5m2`` (each on its
+    own); each scale is a one-element float32 tensor (tensorwise) or channelwise,
+    A_scale (batch, m, 1) and B_scale (batch, 1, n).  ``dtype``: bfloat16 or
+    float16 output (bfloat16 when omitted; ``out``'s dtype wins)."""
+    torch = _torch()
+    if backend != "auto":
+        raise Fp8gError(ERR_UNSUPPORTED, "bmm_fp8",
+                        "only backend='auto' (this library's sm_103a kernel) exists")
+    fmts = {torch.float8_e4m3fn: 0, torch.float8_e5m2: 1}
+    _need(A.dtype in fmts and B.dtype in fmts, "A and B must be float8_e4m3fn or float8_e5m2")
+    _need(A.dim() == 3 and B.dim() == 3, "A must be (batch, m, k) and B (batch, k, n)")
+    batch, m, k = A.shape
+    n = B.shape[2]
+    _need(tuple(B.shape[:2]) == (batch, k), "B must be (%d, %d, n)" % (batch, k))
+    a_ch = A_scale.numel() != 1
+    b_ch = B_scale.numel() != 1
+    _need(A_scale.dtype == torch.float32 and B_scale.dtype == torch.float32,
+          "scales must be float32")
+    _need(not a_ch or tuple(A_scale.shape) == (batch, m, 1), "channelwise A_scale must be (batch, m, 1)")
+    _need(not b_ch or tuple(B_scale.shape) == (batch, 1, n), "channelwise B_scale must be (batch, 1, n)")
+    if out is None:
+        out = torch.empty((batch, m, n), device=A.device,
+                          dtype=dtype if dtype is not None else torch.bfloat16)
+    _need(tuple(out.shape) == (batch, m, n), "out must be (batch, m, n)")
+    code = _out_code(out.dtype)
+    _need(code in (OUT_BF16, OUT_F16), "bmm_fp8 output must be bfloat16 or float16")
+    dev = _cuda_contig((A, B, A_scale, B_scale, out), ("A", "B", "A_scale", "B_scale", "out"))
+    rc = load().bmm_fp8(_ptr(A), _ptr(B), fmts[A.dtype], fmts[B.dtype], _ptr(A_scale), int(a_ch),
+                        _ptr(B_scale), int(b_ch), _ptr(out), code, batch, m, n, k,
+                        _stream_handle(stream, dev))
+    _raise_on(rc, "bmm_fp8")
     return out
 
 

@@ -18,6 +18,7 @@
 #include <string>
 
 #include "fp8g.h"
+#include "bmm_kernel.cuh"
 #include "gemm_kernel.cuh"
 #include "moe.cuh"
 #include "norm_quant.cuh"
@@ -49,8 +50,8 @@ fp8g_status_t cuda_fail(cudaError_t e, const char* what) {
 
 constexpr int kMaxDevices = 64;
 // dense bf16, dense f16 (single CTA), grouped, masked, dense bf16, dense f16 (CTA pair),
-// dense E4M3 (single CTA), dense E4M3 (CTA pair)
-constexpr int kNumKernels = 8;
+// dense E4M3 (single CTA), dense E4M3 (CTA pair), bmm bf16, bmm f16
+constexpr int kNumKernels = 10;
 
 struct DeviceState {
     bool probed = false;
@@ -238,6 +239,47 @@ Params base_params(const float* a_scale, const float* b_scale, void* out, int64_
     p.m_blocks = static_cast<int>((rows + tile_m - 1) / tile_m);
     p.band_m = 8;
     return p;
+}
+
+// bmm_fp8 kernel launch (persistent, one CTA per SM) on validated arguments.
+template <typename OutT>
+fp8g_status_t launch_bmm(DeviceState& ds, int slot, const CUtensorMap& map_a,
+                         const CUtensorMap& map_b, const Params& p, int64_t tiles,
+                         cudaStream_t stream) {
+    auto kernel = fp8g::bmm_kernel<OutT>;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!ds.kernel_ready[slot]) {
+            cudaFuncAttributes attr;
+            cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
+            if (attr.numRegs != static_cast<int>(fp8g::LAUNCH_REGS))
+                return fail(FP8G_ERR_UNSUPPORTED,
+                            "kernel built with %d registers per thread, expected %u", attr.numRegs,
+                            fp8g::LAUNCH_REGS);
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(fp8g::BMM_SMEM_BYTES));
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+            ds.resident[slot] = ds.sm_count;
+            ds.kernel_ready[slot] = true;
+        }
+    }
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    const int64_t units = tiles < ds.resident[slot] ? tiles : ds.resident[slot];
+    cfg.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
+    cfg.blockDim = dim3(fp8g::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = fp8g::BMM_SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    (void)cudaGetLastError();
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return FP8G_OK;
 }
 
 // Contiguous grouped GEMM on validated arguments (m > 0).
@@ -598,6 +640,54 @@ fp8g_status_t fused_add_rmsnorm_fp8_block_quant(void* out, float* block_scale, v
         if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
         t_last_error.clear();
         return FP8G_OK;
+    } catch (...) {
+        return fail(FP8G_ERR_CUDA, "unexpected exception");
+    }
+}
+
+fp8g_status_t bmm_fp8(const void* a, const void* b, fp8g_fp8_format_t a_format,
+                      fp8g_fp8_format_t b_format, const float* a_scale, int a_channelwise,
+                      const float* b_scale, int b_channelwise, void* out,
+                      fp8g_dtype_t out_dtype, int64_t batch, int64_t m, int64_t n, int64_t k,
+                      cudaStream_t stream) {
+    try {
+        if (batch < 0 || m < 0)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "batch = %lld and m = %lld must be >= 0",
+                        (long long)batch, (long long)m);
+        if ((a_format != FP8G_FP8_E4M3 && a_format != FP8G_FP8_E5M2) ||
+            (b_format != FP8G_FP8_E4M3 && b_format != FP8G_FP8_E5M2))
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "operand formats must be E4M3 or E5M2");
+        if (out_dtype != FP8G_OUT_BF16 && out_dtype != FP8G_OUT_F16)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "out_dtype %d is neither BF16 nor FP16",
+                        (int)out_dtype);
+        fp8g_status_t s = check_nk(n, k);
+        if (s != FP8G_OK) return s;
+        if (batch * m > kMaxDim || batch * k > kMaxDim || batch * n > kMaxDim)
+            return fail(FP8G_ERR_UNSUPPORTED, "batch * m, batch * k, batch * n must be < 2^31");
+        const int64_t m_blocks = (m + 127) / 128, n_tiles = (n + 255) / 256;
+        const int64_t tiles = batch * m_blocks * n_tiles;
+        if (tiles > kMaxDim) return fail(FP8G_ERR_UNSUPPORTED, "problem has too many tiles");
+        if (tiles == 0) {
+            t_last_error.clear();
+            return FP8G_OK;
+        }
+        if ((s = check_ptrs(a, b, a_scale, b_scale, out)) != FP8G_OK) return s;
+        DeviceState* ds = nullptr;
+        if ((s = device_state(&ds)) != FP8G_OK) return s;
+        CUtensorMap map_a, map_b;
+        if ((s = encode_map(&map_a, a, batch * m, k, fp8g::BLOCK_M, "a")) != FP8G_OK) return s;
+        // B stays N-major: rows are k (of every batch), 128-column boxes
+        if ((s = encode_map(&map_b, b, batch * k, n, 128, "b")) != FP8G_OK) return s;
+        Params p = base_params(a_scale, b_scale, out, m, n, k);
+        p.num_tiles = static_cast<int>(tiles);
+        p.batch = static_cast<int>(batch);
+        p.a_channelwise = a_channelwise != 0;
+        p.b_channelwise = b_channelwise != 0;
+        p.idesc = fp8g::idesc_bmm(static_cast<uint32_t>(a_format), static_cast<uint32_t>(b_format));
+        p.status = ds->status;
+        if (out_dtype == FP8G_OUT_BF16)
+            return launch_bmm<__nv_bfloat16>(*ds, 8, map_a, map_b, p, tiles, stream);
+        return launch_bmm<__half>(*ds, 9, map_a, map_b, p, tiles, stream);
     } catch (...) {
         return fail(FP8G_ERR_CUDA, "unexpected exception");
     }

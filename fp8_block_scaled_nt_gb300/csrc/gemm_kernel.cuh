@@ -113,6 +113,10 @@ struct Params {
     int scale_mn_major;  // dense form only
     const float* out_scale;  // dense form with E4M3 output: the output's FP32 scale
     int band_m;          // m-blocks per raster band (dense/grouped)
+    // bmm_fp8 (bmm_kernel.cuh): rows = m of one batch, k of one batch
+    int batch;
+    int a_channelwise, b_channelwise;  // scales per row of A / column of B, else one value
+    uint32_t idesc;                    // instruction descriptor (operand formats)
 };
 
 // One output tile as every role of one CTA sees it.

@@ -67,6 +67,9 @@ typedef enum { FP8G_SCALE_K_MAJOR = 0, FP8G_SCALE_MN_MAJOR = 1 } fp8g_scale_majo
  * per-tensor FP32 output scale (the page's output_scale path). */
 typedef enum { FP8G_OUT_BF16 = 0, FP8G_OUT_F16 = 1, FP8G_OUT_E4M3 = 2 } fp8g_dtype_t;
 
+/* FP8 formats of bmm_fp8's operands. */
+typedef enum { FP8G_FP8_E4M3 = 0, FP8G_FP8_E5M2 = 1 } fp8g_fp8_format_t;
+
 /* Bits of the device status word (see fp8g_get_device_status). */
 #define FP8G_DEVICE_TIMEOUT 0x1u          /* a pipeline wait exceeded its limit; the launch gave up */
 #define FP8G_DEVICE_BAD_M_INDICES 0x2u    /* a 128-row block broke the contiguous-layout precondition; skipped */
@@ -99,6 +102,29 @@ fp8g_status_t fp8_gemm_nt_groupwise(const void* a, const void* b,
                                     fp8g_scale_major_t scale_major,
                                     int gran_m, int gran_n, int gran_k,
                                     int mma_sm, cudaStream_t stream);
+
+/*
+ * Batched FP8 GEMM with tensorwise or channelwise scales (page: bmm_fp8).
+ *
+ *   a        (batch, m, k) FP8 codes, row-major; format a_format (E4M3 or E5M2).
+ *   b        (batch, k, n) FP8 codes, row-major; format b_format.  The operation
+ *            is a[b] @ b[b] (B is not transposed, unlike the NT forms above).
+ *   a_scale  FP32: one value (a_channelwise == 0) or (batch, m, 1), one per row of a.
+ *   b_scale  FP32: one value (b_channelwise == 0) or (batch, 1, n), one per column of b.
+ *   out      (batch, m, n) row-major, BF16 or FP16; every element is written.
+ *
+ *   out[b][i][j] = round( (sum_t a[b][i][t] * b[b][t][j]) * a_scale(b, i) * b_scale(b, j) )
+ *
+ * The sum over k is accumulated in FP32 on the tensor cores (no per-block
+ * promotion is needed, as the scales do not depend on k) and scaled once.
+ * n and k must be positive multiples of 128; batch and m may be 0.  a, b, out
+ * 16-byte aligned, scales 4-byte aligned.
+ */
+fp8g_status_t bmm_fp8(const void* a, const void* b, fp8g_fp8_format_t a_format,
+                      fp8g_fp8_format_t b_format, const float* a_scale, int a_channelwise,
+                      const float* b_scale, int b_channelwise, void* out,
+                      fp8g_dtype_t out_dtype, int64_t batch, int64_t m, int64_t n, int64_t k,
+                      cudaStream_t stream);
 
 /*
  * Contiguous grouped FP8 NT GEMM for MoE experts

@@ -46,6 +46,8 @@ CONFIGS = {
     # the producer of the GEMM's activations: 4096 tokens of hidden size 7168
     # (the k of the MoE workloads above)
     "norm_quant_4096x7168": dict(kind="norm", rows=4096, hidden=7168, eps=1e-6, seed=1006),
+    # bmm_fp8: 4 batches of 4096 x 4096 x 7168, E4M3, tensorwise scales
+    "bmm_fp8_b4_4096x4096x7168": dict(kind="bmm", batch=4, m=4096, n=4096, k=7168, seed=1009),
     # the DeepSeek FP8 block-scale MoE layer around the grouped GEMM: fc1 is the
     # grouped workload above (n = 2 * inter = 4096, k = hidden = 7168), fc2 has
     # n = 7168, k = 2048
@@ -210,6 +212,24 @@ def moe(tokens, top_k, num_experts, hidden, inter, seed, scale_exp=(-7.0, -5.0),
                 num_experts=num_experts, hidden=hidden, inter=inter)
 
 
+def bmm(batch, m, n, k, seed, a_fmt="e4m3", b_fmt="e4m3", device="cpu", **_):
+    """Operands of bmm_fp8: A (batch, m, k) and B (batch, k, n) FP8 codes of
+    N(0, 1) values (E4M3 or E5M2, as torch float8 tensors), one tensorwise FP32
+    scale each (2**U(-6, 0))."""
+    gen = generator(seed, device)
+    dts = {"e4m3": (torch.float8_e4m3fn, 448.0), "e5m2": (torch.float8_e5m2, 57344.0)}
+    out = {}
+    for name, shape, fmt in (("A", (batch, m, k), a_fmt), ("B", (batch, k, n), b_fmt)):
+        x = torch.empty(shape, dtype=torch.float32, device=device)
+        x.normal_(0.0, 1.0, generator=gen)
+        dt, lim = dts[fmt]
+        out[name] = x.clamp_(-lim, lim).to(dt)
+    out["A_scale"] = log_uniform((1,), -6.0, 0.0, gen, device)
+    out["B_scale"] = log_uniform((1,), -6.0, 0.0, gen, device)
+    out.update(batch=batch, m=m, n=n, k=k)
+    return out
+
+
 def make(name, device="cpu", **overrides):
     """Operands of one of the named workloads."""
     cfg = dict(CONFIGS[name])
@@ -225,6 +245,8 @@ def make(name, device="cpu", **overrides):
         return norm(device=device, **cfg)
     if kind == "moe":
         return moe(device=device, **cfg)
+    if kind == "bmm":
+        return bmm(device=device, **cfg)
     raise ValueError(kind)
 
 
