@@ -129,6 +129,25 @@ fp8g_status_t encode_map(CUtensorMap* map, const void* base, int64_t rows, int64
     return FP8G_OK;
 }
 
+// Row-major output of `rows` x `n` elements of `esz` bytes as a 2-D TMA view for
+// bulk stores: boxes of `box_rows` rows x 128 bytes, 128-byte swizzle (the
+// layout of the kernel's staging).
+fp8g_status_t encode_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t n, int esz,
+                             int box_rows) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(n * esz)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t elem_strides[2] = {1, 1};
+    CUresult r = g_encode(map, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                          2, base, dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FP8G_ERR_CUDA, "cuTensorMapEncodeTiled(out) failed with CUresult %d",
+                    static_cast<int>(r));
+    return FP8G_OK;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
@@ -214,10 +233,18 @@ fp8g_status_t launch(DeviceState& ds, int slot, const CUtensorMap& map_a, const 
             ds.kernel_ready[slot] = true;
         }
     }
+    // the 2-D view of out: rows of all groups (masked form) or of the form
+    CUtensorMap map_out, map_out_tile;
+    const int64_t out_rows =
+        FORM == fp8g::FORM_MASKED ? static_cast<int64_t>(p.num_groups) * p.rows : p.rows;
+    fp8g_status_t s = encode_out_map(&map_out, p.out, out_rows, p.n, sizeof(OutT), 8);
+    if (s == FP8G_OK)
+        s = encode_out_map(&map_out_tile, p.out, out_rows, p.n, sizeof(OutT), fp8g::BLOCK_M);
+    if (s != FP8G_OK) return s;
     const int64_t units = max_tiles < ds.resident[slot] ? max_tiles : ds.resident[slot];
     cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? 2 * units : units), 1, 1);
     (void)cudaGetLastError();
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, map_out, map_out_tile, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     t_last_error.clear();

@@ -12,17 +12,24 @@
 //   warps 1-2   MMA issuers (even / odd K blocks): 4 x tcgen05.mma (K = 32)
 //               write the block's partial sums P into TMEM buffer 0 / 1 (FP32,
 //               128 lanes x 256 cols), fresh for every K block.
-//   warp 3      idle (it completes the first warpgroup).
-//   warps 4-11  promotion + epilogue: read the partial from TMEM, multiply by
+//   warp 3      storer (dense form): copies each finished tile from its
+//               shared-memory staging to global memory with bulk tensor
+//               stores; idle in the grouped and masked forms.
+//   warps 4-11  promotion: read the partial from TMEM, multiply by
 //               a_scale(row,kb) * b_scale(col block,kb) and accumulate in FP32
 //               registers (one row per thread, 128 columns per warpgroup);
-//               after the last K block round to BF16/FP16 through a shared-memory
-//               staging slice and store whole 128-byte row segments.
+//               after the last K block round the row to BF16/FP16 (or E4M3)
+//               into the staging.  Dense form: hand the staging to the storer
+//               and go on with the next tile at once; grouped and masked
+//               forms: store the staged rows as whole 128-byte row segments
+//               (rows outside the form skipped), 64 columns at a time.
 // The 128 x 256 FP32 running sums take half of the register file, so the
 // control warpgroup hands registers to the two promotion warpgroups
 // (setmaxnreg: 40 + 2 x 232 per thread, exactly the launch's 3 x 168).
 // The two TMEM buffers let the tensor cores compute block kb+1 while block kb
-// is being promoted, and the next tile's first blocks while the epilogue runs.
+// is being promoted.  In the dense form the staging holds a whole tile, so the
+// global stores of tile i overlap the promotion of tile i+1 (the storer has a
+// whole tile's time to empty it).
 //
 // Two variants of the pipeline:
 //   single CTA  (PAIR = false): a 128 x 256 tile per CTA; the producer loads
@@ -31,7 +38,7 @@
 //   CTA pair    (PAIR = true, dense form): a cluster of two CTAs computes a
 //               256 x 256 tile with tcgen05.mma.cta_group::2 (M = 256).  Each
 //               CTA loads its own 128 rows of A and its half (128 rows) of B,
-//               32 KB per K block into 5 slots, so every SM moves a third less
+//               32 KB per K block into 4 slots, so every SM moves a third less
 //               data through L2 and shared memory per MMA.  The even CTA issues
 //               the MMAs and multicasts their completion to both CTAs; the odd
 //               CTA's MMA warp relays "my slot has landed" to the even CTA, and
@@ -67,11 +74,17 @@ constexpr uint32_t PROMO_REGS = 232;    // warpgroups 1-2 after setmaxnreg.inc
 static_assert(128 * CONTROL_REGS + 256 * PROMO_REGS <= NUM_THREADS * LAUNCH_REGS,
               "register split exceeds the launch's registers");
 constexpr uint32_t TMEM_COLS = 2 * BLOCK_N;  // two FP32 partial buffers
-constexpr int BAR_BYTES = 256;               // barriers, TMEM slot, abort flag
-// Output staging: each promotion warpgroup rounds 128 rows x 64 columns at a
-// time into 128-byte rows of shared memory before the warps store them.
+constexpr int BAR_BYTES = 256;  // barriers, TMEM slot, abort flag, storer descriptor
+// Output staging of the bmm kernel: each epilogue warpgroup rounds 128 rows x
+// 64 columns at a time into 128-byte rows of shared memory before its warps
+// store them.
 constexpr int OUT_COLS = 64;
 constexpr int OUT_STAGE_BYTES = BLOCK_M * OUT_COLS * 2;  // 16 KB per warpgroup
+// Output staging of the GEMM kernel: a promotion warpgroup's whole tile share,
+// 128 rows x 128 columns, as 128-byte rows (two 64-column slices for BF16/FP16,
+// one 128-column slice for E4M3).
+constexpr int TILE_STAGE_BYTES = BLOCK_M * 128 * 2;  // 32 KB per warpgroup
+constexpr int STAGE_SLICE_BYTES = BLOCK_M * 128;     // one slice of 128-byte rows
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
 constexpr uint64_t ABORT_GRACE_NS = 5000000ull;  // 5 ms
@@ -81,18 +94,25 @@ enum Form { FORM_DENSE = 0, FORM_GROUPED = 1, FORM_MASKED = 2 };
 // Geometry of the pipeline variants.  Ring depths: shared memory left over
 // becomes L1, which the per-row scale loads of the promotion warps live on, so
 // the rings are as deep as the copies need and no deeper (measured); the
-// HBM-bound masked form keeps one more slot in flight.
+// HBM-bound masked form keeps one more slot in flight.  The dense form hands
+// finished tiles to the storer warp through a whole-tile staging (measured:
+// +4% on 4096 x 7168 x 2048); the grouped and masked forms keep the shared
+// memory for L1 and their rings and store from the promotion warps (the
+// storer cost them 1% and 4%).
 template <bool PAIR, int FORM>
 struct Cfg {
     static constexpr int TILE_M = PAIR ? 2 * BLOCK_M : BLOCK_M;  // rows of a scheduled tile
     static constexpr int B_ROWS = PAIR ? BLOCK_N / 2 : BLOCK_N;  // B rows one CTA loads
-    static constexpr int STAGES = PAIR ? 5 : (FORM == FORM_MASKED ? 4 : 3);
+    static constexpr int STAGES = PAIR ? 4 : (FORM == FORM_MASKED ? 4 : 3);
+    static constexpr bool STORER = FORM == FORM_DENSE;
+    static constexpr int OUT_BYTES = STORER ? TILE_STAGE_BYTES : OUT_STAGE_BYTES;  // per half
     static constexpr int A_BYTES = BLOCK_M * BLOCK_K;
     static constexpr int B_BYTES = B_ROWS * BLOCK_K;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr size_t SMEM_BYTES = 1024 /* alignment slack */ +
-                                         size_t(STAGES) * STAGE_BYTES + 2 * OUT_STAGE_BYTES +
+                                         size_t(STAGES) * STAGE_BYTES + 2 * OUT_BYTES +
                                          BAR_BYTES;
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static constexpr uint32_t IDESC = idesc_e4m3_f32(TILE_M, BLOCK_N);
 };
 
@@ -521,21 +541,206 @@ __device__ __forceinline__ void store_tile_rows(OutT* out, int64_t n, int64_t ro
     }
 }
 
+// Rounds one promotion thread's row (thread r holds row r of its warpgroup;
+// acc[i] = columns 2i, 2i+1) into the warpgroup's tile staging: 128-byte rows,
+// 16-byte chunk c of row r at chunk c ^ (r % 8) so that the 32 rows a warp
+// writes at once, and the 4 rows the storer reads at once, spread over all
+// banks.  BF16/FP16: slice 0 holds columns 0-63, slice 1 columns 64-127;
+// E4M3: slice 0 holds the codes of value * out_inv of all 128 columns.
+template <typename OutT>
+__device__ __forceinline__ void stage_tile_row(uint8_t* staging, const uint64_t (&acc)[64],
+                                               float out_inv) {
+    constexpr int ESZ = static_cast<int>(sizeof(OutT));
+    const int r = ((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31);
+    const uint32_t base = smem_u32(staging) + r * 128;
+    OutT* tag = nullptr;
+    (void)tag;
+    (void)out_inv;
+#pragma unroll
+    for (int slice = 0; slice < ESZ; ++slice) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint4 v;
+            if constexpr (ESZ == 2) {
+                const int a = slice * 32 + 4 * c;  // 8 values
+                v.x = pack2(lo_f32(acc[a + 0]), hi_f32(acc[a + 0]), tag);
+                v.y = pack2(lo_f32(acc[a + 1]), hi_f32(acc[a + 1]), tag);
+                v.z = pack2(lo_f32(acc[a + 2]), hi_f32(acc[a + 2]), tag);
+                v.w = pack2(lo_f32(acc[a + 3]), hi_f32(acc[a + 3]), tag);
+            } else {
+                const int a = 8 * c;  // 16 values
+                v.x = pack4_e4m3(lo_f32(acc[a + 0]), hi_f32(acc[a + 0]), lo_f32(acc[a + 1]),
+                                 hi_f32(acc[a + 1]), out_inv);
+                v.y = pack4_e4m3(lo_f32(acc[a + 2]), hi_f32(acc[a + 2]), lo_f32(acc[a + 3]),
+                                 hi_f32(acc[a + 3]), out_inv);
+                v.z = pack4_e4m3(lo_f32(acc[a + 4]), hi_f32(acc[a + 4]), lo_f32(acc[a + 5]),
+                                 hi_f32(acc[a + 5]), out_inv);
+                v.w = pack4_e4m3(lo_f32(acc[a + 6]), hi_f32(acc[a + 6]), lo_f32(acc[a + 7]),
+                                 hi_f32(acc[a + 7]), out_inv);
+            }
+            st_shared_v4(base + slice * STAGE_SLICE_BYTES + ((c ^ (r & 7)) << 4), v);
+        }
+    }
+}
+
+// What a promotion warpgroup hands the storer with each staged tile share.
+struct StageDesc {
+    int32_t x[2];          // per half: first output column of the share
+    int32_t y[2];          // per half: output row of tile row 0 (2-D view of out), or
+                           // STAGE_END once the warpgroup has no more tiles
+    uint32_t row_mask[8];  // [half][quarter]: bit L = row 32 quarter + L is stored
+};
+constexpr int32_t STAGE_END = -1;
+
+// Warp 3: serves the two promotion warpgroups in turn, one staged tile share
+// at a time, and hands the staging back.  A share whose 128 rows are all
+// stored goes out as one bulk tensor store per 128-byte column slice
+// (`map_out_tile`: 128-row boxes); otherwise every 8-row group whose rows are
+// all stored goes out as one (`map_out`: 8-row boxes, the staging's 1 KB
+// swizzle atoms), and the rows of the other groups that belong to the form are
+// stored by the warp, four 128-byte row segments per instruction.  Lane 0
+// issues the bulk stores.  Both
+// warpgroups walk the same tiles, so each stages one share per tile and then
+// STAGE_END; the storer stops when both have ended (or on an abort), after its
+// bulk stores have completed.
+template <typename OutT>
+__device__ __forceinline__ void run_storer(const CUtensorMap* map_out,
+                                           const CUtensorMap* map_out_tile, OutT* out, int64_t n,
+                                           uint8_t* sOut, uint64_t* out_full, uint64_t* out_empty,
+                                           const StageDesc* desc, const Ctl& ctl) {
+    constexpr int ESZ = static_cast<int>(sizeof(OutT));
+    constexpr int SLICE_COLS = 128 / ESZ;  // output columns of one 128-byte row
+    const int lane = threadIdx.x & 31;
+    const int chunk = lane & 7, sub = lane >> 3;
+    const volatile StageDesc* vd = desc;
+    uint32_t sphase = 0;  // bit h: parity of the next phase of out_full[h]
+    uint32_t live = 3;    // bit h: warpgroup h has not ended
+    for (int h = 0; live; h ^= 1) {
+        if (!((live >> h) & 1u)) continue;
+        if (!warp_wait(out_full + h, (sphase >> h) & 1u, ctl)) break;
+        sphase ^= 1u << h;
+        const int32_t y0 = vd->y[h];
+        if (y0 == STAGE_END) {
+            live &= ~(1u << h);
+            continue;
+        }
+        const int32_t x0 = vd->x[h];
+        const uint32_t base = smem_u32(sOut + h * TILE_STAGE_BYTES);
+        uint32_t groups = 0;  // bit g: rows 8g .. 8g+7 are all stored
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t okm = vd->row_mask[h * 4 + q];
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                if (((okm >> (8 * b)) & 0xFFu) == 0xFFu) groups |= 1u << (4 * q + b);
+        }
+        if (lane == 0) {
+            if (groups == 0xFFFFu) {  // every row: one 128-row box per slice
+                for (int slice = 0; slice < ESZ; ++slice)
+                    tma_store_2d(map_out_tile, base + slice * STAGE_SLICE_BYTES,
+                                 x0 + slice * SLICE_COLS, y0);
+            } else {
+#pragma unroll 1
+                for (int g = 0; g < 16; ++g)
+                    if ((groups >> g) & 1u)
+                        for (int slice = 0; slice < ESZ; ++slice)
+                            tma_store_2d(map_out, base + slice * STAGE_SLICE_BYTES + g * 1024,
+                                         x0 + slice * SLICE_COLS, y0 + 8 * g);
+            }
+            bulk_commit_group();
+        }
+        if (groups != 0xFFFFu) {
+            uint8_t* d = reinterpret_cast<uint8_t*>(out + static_cast<int64_t>(y0) * n + x0) +
+                         chunk * 16;
+            const int64_t row_bytes = n * ESZ;
+#pragma unroll 1
+            for (int slice = 0; slice < ESZ; ++slice) {
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t okm = vd->row_mask[h * 4 + q];
+#pragma unroll 1
+                    for (int j = 0; j < 8; ++j) {
+                        const int rr = q * 32 + 4 * j + sub;  // the 4 rows share an 8-row group
+                        if ((groups >> (rr >> 3)) & 1u) continue;  // stored in bulk
+                        const uint4 v = ld_shared_v4(base + slice * STAGE_SLICE_BYTES + rr * 128 +
+                                                     ((chunk ^ (rr & 7)) << 4));
+                        if ((okm >> (4 * j + sub)) & 1u)
+                            *reinterpret_cast<uint4*>(d + rr * row_bytes + slice * 128) = v;
+                    }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_read_all();  // the staging has been read
+        __syncwarp();
+        if (lane == 0) mbar_arrive(out_empty + h);
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+}
+
 // One scale of K block kb (0 where the row or column block is outside the form).
 __device__ __forceinline__ float load_scale(const float* x, int step, int kb) {
     return x ? __ldg(x + static_cast<int64_t>(kb) * step) : 0.0f;
 }
 
+// Where a promotion thread finds its scales and its output row in a tile.
+struct RowScales {
+    const float* sa;       // a_scale of the row at K block 0 (null outside the form)
+    const float* sb;       // b_scale of the 128-column block at K block 0 (null outside)
+    int sa_step, sb_step;  // floats from one K block to the next
+    int64_t out_row;       // row of the 2-D view of out
+    bool row_ok;           // the row belongs to the form (is stored)
+    bool col_ok;           // the warpgroup's 128 columns exist
+};
+
+template <int FORM>
+__device__ __forceinline__ RowScales row_scales(const Params& p, const Tile& tile, int r,
+                                                int quarter, int half) {
+    const int KB = p.kblocks;
+    const int jb = tile.nb * (BLOCK_N / 128) + half;  // 128-column scale block
+    RowScales x;
+    x.col_ok = jb < p.nblocks;
+    x.sa = x.sb = nullptr;
+    x.sa_step = x.sb_step = 1;
+    if constexpr (FORM == FORM_MASKED) {
+        const int rin = tile.mb * BLOCK_M + r;
+        x.out_row = static_cast<int64_t>(tile.group) * p.rows + rin;
+        x.row_ok = rin < tile.group_rows;
+        if (rin < p.rows) x.sa = p.a_scale + x.out_row * KB;
+        if (x.col_ok) x.sb = p.b_scale + (static_cast<int64_t>(tile.group) * p.nblocks + jb) * KB;
+    } else {
+        x.out_row = static_cast<int64_t>(tile.row0) + r;
+        const bool row_in = x.out_row < p.rows;
+        if constexpr (FORM == FORM_GROUPED) {
+            x.row_ok = row_in && tile.row_expert[quarter] == tile.group;
+            if (row_in) x.sa = p.a_scale + x.out_row * KB;
+            if (x.col_ok)
+                x.sb = p.b_scale + (static_cast<int64_t>(tile.group) * p.nblocks + jb) * KB;
+        } else {
+            x.row_ok = row_in;
+            if (p.scale_mn_major) {
+                if (row_in) x.sa = p.a_scale + x.out_row, x.sa_step = p.rows;
+                if (x.col_ok) x.sb = p.b_scale + jb, x.sb_step = p.nblocks;
+            } else {
+                if (row_in) x.sa = p.a_scale + x.out_row * KB;
+                if (x.col_ok) x.sb = p.b_scale + static_cast<int64_t>(jb) * KB;
+            }
+        }
+    }
+    return x;
+}
+
 template <int FORM, typename OutT, bool PAIR>
 __device__ __forceinline__ void run_promotion(const Params& p, int rank, uint64_t* acc_full,
                                               uint64_t* acc_empty, uint32_t tmem_base,
-                                              uint8_t* sOut, const Ctl& ctl) {
+                                              uint8_t* sOut, uint64_t* out_full,
+                                              uint64_t* out_empty, StageDesc* desc,
+                                              const Ctl& ctl) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quarter = warp & 3;       // this warp may read TMEM lanes 32*quarter .. +31
     const int half = (warp - FIRST_PROMO_WARP) >> 2;  // which 128 columns of the tile
     const int r = quarter * 32 + lane;  // row of the tile owned by this thread
     const int KB = p.kblocks;
-    OutT* out = static_cast<OutT*>(p.out);
     Scheduler<FORM, PAIR> sched(p, rank);
     // E4M3 output: codes of value / out_scale, computed as value * (1 / out_scale)
     float out_inv = 1.0f;
@@ -546,45 +751,20 @@ __device__ __forceinline__ void run_promotion(const Params& p, int rank, uint64_
         release0 = mapa_shared(acc_empty + 0, 0);
         release1 = mapa_shared(acc_empty + 1, 0);
     }
+    using C = Cfg<PAIR, FORM>;
     int buf = 0;
-    uint32_t bphase = 0;
+    uint32_t bphase = 0, ephase = 0;
+    uint8_t* staging = sOut + half * C::OUT_BYTES;
+    bool aborted = false;
     for (int t = tile_first<PAIR>();; t += tile_stride<PAIR>()) {
         Tile tile;
         if (!sched.next(t, tile, false)) break;
         if (tile.skip) continue;
 
-        const int jb = tile.nb * (BLOCK_N / 128) + half;  // 128-column scale block
-        const bool col_ok = jb < p.nblocks;
-        const int col0 = tile.nb * BLOCK_N + half * 128;
-        int64_t out_row;
-        bool row_ok;
-        const float *sa = nullptr, *sb = nullptr;
-        int sa_step = 1, sb_step = 1;
-        if constexpr (FORM == FORM_MASKED) {
-            const int rin = tile.mb * BLOCK_M + r;
-            out_row = static_cast<int64_t>(tile.group) * p.rows + rin;
-            row_ok = rin < tile.group_rows;
-            if (rin < p.rows) sa = p.a_scale + out_row * KB;
-            if (col_ok) sb = p.b_scale + (static_cast<int64_t>(tile.group) * p.nblocks + jb) * KB;
-        } else {
-            out_row = static_cast<int64_t>(tile.row0) + r;
-            const bool row_in = out_row < p.rows;
-            if constexpr (FORM == FORM_GROUPED) {
-                row_ok = row_in && tile.row_expert[quarter] == tile.group;
-                if (row_in) sa = p.a_scale + out_row * KB;
-                if (col_ok)
-                    sb = p.b_scale + (static_cast<int64_t>(tile.group) * p.nblocks + jb) * KB;
-            } else {
-                row_ok = row_in;
-                if (p.scale_mn_major) {
-                    if (row_in) sa = p.a_scale + out_row, sa_step = p.rows;
-                    if (col_ok) sb = p.b_scale + jb, sb_step = p.nblocks;
-                } else {
-                    if (row_in) sa = p.a_scale + out_row * KB;
-                    if (col_ok) sb = p.b_scale + static_cast<int64_t>(jb) * KB;
-                }
-            }
-        }
+        const RowScales rs = row_scales<FORM>(p, tile, r, quarter, half);
+        const bool col_ok = rs.col_ok, row_ok = rs.row_ok;
+        const float *sa = rs.sa, *sb = rs.sb;
+        const int sa_step = rs.sa_step, sb_step = rs.sb_step;
 
         uint64_t acc[64];  // FP32 running sums, two columns per register pair
 #pragma unroll
@@ -643,19 +823,55 @@ __device__ __forceinline__ void run_promotion(const Params& p, int rank, uint64_
                 bphase ^= 1u;
             }
         }
-        // Every warp of the warpgroup takes part in the epilogue's barriers, also
-        // after an abort (then storing nothing); the warpgroup stops together.
-        if (col_ok)  // uniform over the warpgroup
-            store_tile_rows<OutT>(out, p.n, out_row - r, col0, ok && row_ok, acc,
-                                  sOut + half * OUT_STAGE_BYTES, 1 + half, out_inv);
-        if (named_barrier_or(1 + half, 128, !ok)) break;
+        if constexpr (!C::STORER) {
+            // Every warp of the warpgroup takes part in the epilogue's
+            // barriers, also after an abort (then storing nothing); the
+            // warpgroup stops together.
+            if (col_ok)  // uniform over the warpgroup
+                store_tile_rows<OutT>(static_cast<OutT*>(p.out), p.n, rs.out_row - r,
+                                      tile.nb * BLOCK_N + half * 128, ok && row_ok, acc, staging,
+                                      1 + half, out_inv);
+            if (named_barrier_or(1 + half, 128, !ok)) break;
+            continue;
+        }
+        // Stage the rounded row for the storer once it has emptied this
+        // warpgroup's previous share (a half without columns stages no rows).
+        // After an abort nothing is staged (the storer's wait then ends with
+        // the abort); every warp still joins the vote, so the warpgroup stops
+        // together.
+        if (ok && warp_wait(out_empty + half, ephase ^ 1u, ctl)) {
+            if (col_ok) {  // uniform
+                stage_tile_row<OutT>(staging, acc, out_inv);
+                fence_proxy_async_shared();  // the storer's bulk stores read it
+            }
+            const uint32_t m = __ballot_sync(0xffffffffu, row_ok && col_ok);
+            if (lane == 0) desc->row_mask[half * 4 + quarter] = m;
+            if (quarter == 0 && lane == 0) {
+                desc->x[half] = tile.nb * BLOCK_N + half * 128;
+                desc->y[half] = static_cast<int32_t>(rs.out_row - r);
+            }
+            mbar_arrive(out_full + half);
+        } else {
+            ok = false;
+        }
+        ephase ^= 1u;
+        if (named_barrier_or(1 + half, 128, !ok)) {
+            aborted = true;
+            break;
+        }
+    }
+    // No more tiles: tell the storer (after it has emptied the last share).
+    if (C::STORER && !aborted && warp_wait(out_empty + half, ephase ^ 1u, ctl)) {
+        if (quarter == 0 && lane == 0) desc->y[half] = STAGE_END;
+        mbar_arrive(out_full + half);
     }
 }
 
 template <int FORM, typename OutT, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                const Params p) {
+                const __grid_constant__ CUtensorMap map_out,
+                const __grid_constant__ CUtensorMap map_out_tile, const Params p) {
     using C = Cfg<PAIR, FORM>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -663,13 +879,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::STAGES * C::A_BYTES;
     uint8_t* sOut = sB + C::STAGES * C::B_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 2 * OUT_STAGE_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 2 * C::OUT_BYTES);
     uint64_t* empty = full + C::STAGES;
     uint64_t* acc_full = empty + C::STAGES;
     uint64_t* acc_empty = acc_full + 2;
-    uint64_t* drain = acc_empty + 2;
+    uint64_t* out_full = acc_empty + 2;  // per warpgroup half: its tile share is staged
+    uint64_t* out_empty = out_full + 2;  // per half: the storer has emptied the staging
+    uint64_t* drain = out_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+    StageDesc* stage_desc = reinterpret_cast<StageDesc*>(abort_flag + 1);
 
     const int warp = threadIdx.x >> 5;
     const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
@@ -682,6 +901,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full + b, 1);
             mbar_init(acc_empty + b, PAIR ? 2 * NUM_PROMO_WARPS : NUM_PROMO_WARPS);
+            mbar_init(out_full + b, 128);  // every thread of the promotion warpgroup
+            mbar_init(out_empty + b, 1);
         }
         mbar_init(drain, 2);  // one commit from each MMA-issuing warp
         *abort_flag = 0;
@@ -690,6 +911,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 32) {
         tma_prefetch_map(&map_a);
         tma_prefetch_map(&map_b);
+        tma_prefetch_map(&map_out);
+        tma_prefetch_map(&map_out_tile);
     }
     if (warp == 1) {
         if constexpr (PAIR) {
@@ -730,10 +953,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 run_mma<FORM, false>(p, sA, sB, full, empty, acc_full, acc_empty, drain, tmem_base,
                                      ctl, warp - 1);
             }
+        } else if constexpr (C::STORER) {
+            run_storer<OutT>(&map_out, &map_out_tile, static_cast<OutT*>(p.out), p.n, sOut,
+                             out_full, out_empty, stage_desc, ctl);
         }
     } else {
         regs_inc<PROMO_REGS>();
-        run_promotion<FORM, OutT, PAIR>(p, rank, acc_full, acc_empty, tmem_base, sOut, ctl);
+        run_promotion<FORM, OutT, PAIR>(p, rank, acc_full, acc_empty, tmem_base, sOut, out_full,
+                                        out_empty, stage_desc, ctl);
     }
 
     tc_fence_before_sync();
