@@ -37,6 +37,11 @@ namespace fp8g {
 constexpr int MOE_ROUTE_THREADS = 1024;
 constexpr int MOE_ROW_THREADS = 128;  // per token / per routed row
 constexpr int MOE_MAX_EXPERTS = 4096;
+// Loads a thread issues before it uses the first of them: these kernels are
+// bound by memory latency, so every thread keeps this many reads in flight.
+constexpr int MOE_ROUTE_BATCH = 8;
+constexpr int MOE_ROW_BATCH = 4;
+constexpr int MOE_COMBINE_SLOTS = 8;  // slots whose rows the combine reads at once
 
 __host__ __device__ inline int64_t moe_rows(int64_t tokens, int64_t top_k, int64_t experts) {
     return (tokens * top_k + 127 * experts + 127) / 128 * 128;
@@ -56,12 +61,20 @@ __global__ void __launch_bounds__(MOE_ROUTE_THREADS)
     for (int e = threadIdx.x; e < experts; e += blockDim.x) count[e] = cursor[e] = 0;
     for (int r = threadIdx.x; r < m_rows; r += blockDim.x) m_indices[r] = -1;
     __syncthreads();
-    for (int p = threadIdx.x; p < pairs; p += blockDim.x) {
-        const int e = __ldg(token_selected + p);
-        if (e >= 0 && e < experts)
-            atomicAdd(&count[e], 1);
-        else if (e != -1)
-            atomicOr(status, FP8G_DEVICE_BAD_M_INDICES);
+    for (int p0 = threadIdx.x; p0 < pairs; p0 += blockDim.x * MOE_ROUTE_BATCH) {
+        int e[MOE_ROUTE_BATCH];
+#pragma unroll
+        for (int u = 0; u < MOE_ROUTE_BATCH; ++u) {
+            const int p = p0 + u * blockDim.x;
+            e[u] = p < pairs ? __ldg(token_selected + p) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < MOE_ROUTE_BATCH; ++u) {
+            if (e[u] >= 0 && e[u] < experts)
+                atomicAdd(&count[e[u]], 1);
+            else if (e[u] != -1)
+                atomicOr(status, FP8G_DEVICE_BAD_M_INDICES);
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -72,14 +85,24 @@ __global__ void __launch_bounds__(MOE_ROUTE_THREADS)
         }
     }
     __syncthreads();
-    for (int p = threadIdx.x; p < pairs; p += blockDim.x) {
-        const int e = __ldg(token_selected + p);
-        int row = -1;
-        if (e >= 0 && e < experts) {
-            row = offset[e] + atomicAdd(&cursor[e], 1);
-            m_indices[row] = e;
+    for (int p0 = threadIdx.x; p0 < pairs; p0 += blockDim.x * MOE_ROUTE_BATCH) {
+        int e[MOE_ROUTE_BATCH];
+#pragma unroll
+        for (int u = 0; u < MOE_ROUTE_BATCH; ++u) {
+            const int p = p0 + u * blockDim.x;
+            e[u] = p < pairs ? __ldg(token_selected + p) : -1;
         }
-        row_of[p] = row;
+#pragma unroll
+        for (int u = 0; u < MOE_ROUTE_BATCH; ++u) {
+            const int p = p0 + u * blockDim.x;
+            if (p >= pairs) break;
+            int row = -1;
+            if (e[u] >= 0 && e[u] < experts) {
+                row = offset[e[u]] + atomicAdd(&cursor[e[u]], 1);
+                m_indices[row] = e[u];
+            }
+            row_of[p] = row;
+        }
     }
 }
 
@@ -112,20 +135,31 @@ __global__ void __launch_bounds__(MOE_ROW_THREADS)
     const int lane = threadIdx.x & 31, hl = threadIdx.x & 15;
     const unsigned half_mask = 0xFFFFu << (lane & 16);
     const uint4* in4 = reinterpret_cast<const uint4*>(input + static_cast<int64_t>(t) * hidden);
-    for (int blk = threadIdx.x >> 4; blk < nblk; blk += MOE_ROW_THREADS / 16) {
-        const int v = blk * (NQ_BLOCK / 8) + hl;
-        const uint4 x = ld_once_ro_v4(in4 + v);
-        const uint32_t* xw = reinterpret_cast<const uint32_t*>(&x);
-        float f[8];
+    constexpr int STEP = MOE_ROW_THREADS / 16;  // blocks per pass of the CTA
+    for (int blk0 = threadIdx.x >> 4; blk0 < nblk; blk0 += STEP * MOE_ROW_BATCH) {
+        uint4 x[MOE_ROW_BATCH];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) f[2 * i] = bf16_lo(xw[i]), f[2 * i + 1] = bf16_hi(xw[i]);
-        float scale;
-        const uint2 codes = quantise_block_8(f, half_mask, scale);
-        for (int s = 0; s < top_k; ++s) {
-            const int r = __ldg(row_of + static_cast<int64_t>(t) * top_k + s);
-            if (r < 0) continue;
-            reinterpret_cast<uint2*>(a + static_cast<int64_t>(r) * hidden)[v] = codes;
-            if (hl == 0) a_scale[static_cast<int64_t>(r) * nblk + blk] = scale;
+        for (int u = 0; u < MOE_ROW_BATCH; ++u) {
+            const int blk = blk0 + u * STEP;
+            if (blk < nblk) x[u] = ld_once_ro_v4(in4 + blk * (NQ_BLOCK / 8) + hl);
+        }
+#pragma unroll
+        for (int u = 0; u < MOE_ROW_BATCH; ++u) {
+            const int blk = blk0 + u * STEP;  // uniform over the half-warp
+            if (blk >= nblk) break;
+            const int v = blk * (NQ_BLOCK / 8) + hl;
+            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&x[u]);
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) f[2 * i] = bf16_lo(xw[i]), f[2 * i + 1] = bf16_hi(xw[i]);
+            float scale;
+            const uint2 codes = quantise_block_8(f, half_mask, scale);
+            for (int s = 0; s < top_k; ++s) {
+                const int r = __ldg(row_of + static_cast<int64_t>(t) * top_k + s);
+                if (r < 0) continue;
+                reinterpret_cast<uint2*>(a + static_cast<int64_t>(r) * hidden)[v] = codes;
+                if (hl == 0) a_scale[static_cast<int64_t>(r) * nblk + blk] = scale;
+            }
         }
     }
 }
@@ -172,18 +206,31 @@ __global__ void __launch_bounds__(MOE_ROW_THREADS)
     grid_launch_dependents();
     const int t = blockIdx.x;
     const int nvec = hidden / 8;
+    const int32_t* rows = row_of + static_cast<int64_t>(t) * top_k;
     for (int v = threadIdx.x; v < nvec; v += MOE_ROW_THREADS) {
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int s = 0; s < top_k; ++s) {
-            const int r = __ldg(row_of + static_cast<int64_t>(t) * top_k + s);
-            if (r < 0) continue;
-            const uint4 yv = ld_once_v4(reinterpret_cast<const uint4*>(
-                                            y + static_cast<int64_t>(r) * hidden) + v);
-            const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv);
+        // slots in groups of MOE_COMBINE_SLOTS: all of a group's rows are read
+        // before the first is added (the sum stays in slot order)
+        for (int s0 = 0; s0 < top_k; s0 += MOE_COMBINE_SLOTS) {
+            uint4 yv[MOE_COMBINE_SLOTS];
+            bool live[MOE_COMBINE_SLOTS];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] += bf16_lo(yw[i]);
-                acc[2 * i + 1] += bf16_hi(yw[i]);
+            for (int j = 0; j < MOE_COMBINE_SLOTS; ++j) {
+                const int r = s0 + j < top_k ? __ldg(rows + s0 + j) : -1;
+                live[j] = r >= 0;
+                if (live[j])
+                    yv[j] = ld_once_v4(reinterpret_cast<const uint4*>(
+                                           y + static_cast<int64_t>(r) * hidden) + v);
+            }
+#pragma unroll
+            for (int j = 0; j < MOE_COMBINE_SLOTS; ++j) {
+                if (!live[j]) continue;
+                const uint32_t* yw = reinterpret_cast<const uint32_t*>(&yv[j]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] += bf16_lo(yw[i]);
+                    acc[2 * i + 1] += bf16_hi(yw[i]);
+                }
             }
         }
         uint4 o;
