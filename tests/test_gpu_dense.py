@@ -53,6 +53,36 @@ def test_ragged_shapes_full_parity(fp8g, oracle_mod, mnk, major, out_dtype, mma_
 
 
 @pytest.mark.parametrize("mma_sm", [1, 2])
+@pytest.mark.parametrize("out_kind", ["bf16", "e4m3"])
+@pytest.mark.parametrize("m", [7, 129, 200, 263])
+def test_nothing_written_past_the_last_row(fp8g, m, out_kind, mma_sm):
+    # out is the first m rows of a larger buffer; the rows after it (and the
+    # missing right half of the last 256-column tile, n = 384) must stay as
+    # they were: the last m-block is stored partly by 8-row bulk boxes and
+    # partly row by row
+    n, k = 384, 256
+    w = workloads.dense(m, n, k, seed=m + 5)
+    d = to_device(w)
+    if out_kind == "bf16":
+        buf = torch.full((m + 128, n), -3.0, dtype=torch.bfloat16, device="cuda")
+        fp8g.fp8_gemm_nt_groupwise(d["a"], d["b"], d["a_scale"], d["b_scale"], buf[:m],
+                                   mma_sm=mma_sm)
+        guard = buf[m:].view(torch.int16)
+        untouched = torch.full_like(guard, int(torch.tensor(-3.0).bfloat16().view(torch.int16)))
+    else:
+        buf = torch.full((m + 128, n), 0x7F, dtype=torch.uint8, device="cuda")  # E4M3 NaN
+        scale = torch.ones(1, dtype=torch.float32, device="cuda")
+        fp8g.fp8_gemm_nt_groupwise(d["a"], d["b"], d["a_scale"], d["b_scale"], buf[:m],
+                                   mma_sm=mma_sm, output_scale=scale)
+        guard = buf[m:]
+        untouched = torch.full_like(guard, 0x7F)
+    torch.cuda.synchronize()
+    assert torch.equal(guard, untouched)
+    if out_kind == "e4m3":  # every row of out written (saturated codes are never NaN)
+        assert not (buf[:m] == 0x7F).any()
+
+
+@pytest.mark.parametrize("mma_sm", [1, 2])
 def test_multi_wave_full_parity(fp8g, oracle_mod, mma_sm):
     # more tiles than SMs (or SM pairs), several K blocks, m and n tails
     w = workloads.dense(2100, 2432, 512, seed=77)
