@@ -217,7 +217,8 @@ fp8g_status_t fused_add_rmsnorm_fp8_block_quant(void* out, float* block_scale, v
  *                                                     fused_add_rmsnorm_fp8_block_quant)
  *   for each slot s with e = token_selected[t, s] != -1:
  *     h   = BF16(fc1_e(xq, xs))     rows [0, I) of h are the gate, [I, 2 I) the up part
- *     act = silu(h[0:I]) * h[I:2I]  (FP32), then its 1x128 quantisation
+ *     act = silu(h[0:I]) * h[I:2I]  (FP32; silu with the hardware exponential and
+ *                                    divide), then its 1x128 quantisation
  *     y   = BF16(fc2_e(act))
  *   out[t] = BF16(sum of y over the token's slots)   (no routing weights: the
  *                                                     page's signature has none)
