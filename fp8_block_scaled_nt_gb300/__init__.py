@@ -190,6 +190,12 @@ def fp8_gemm_nt_groupwise(a, b, a_scale, b_scale, out, scale_major="K", mma_sm=1
     _need(tuple(out.shape) == (m, n), "out must be (%d, %d), got %s" % (m, n, tuple(out.shape)))
     _need(a_scale.dtype == torch.float32 and b_scale.dtype == torch.float32, "scales must be float32")
     kb, nb = k // 128, n // 128
+    if b_scale.numel() == 1 and nb * kb != 1:
+        # a scalar b_scale (the page allows one: only a non-scalar tensor must be
+        # contiguous) scales every block of b alike: it is handed to the library
+        # as that value on the whole (n/128, k/128) block grid
+        grid = (nb, kb) if scale_major in (None, "K") else (kb, nb)
+        b_scale = b_scale.reshape(1, 1).expand(*grid).contiguous()
     if scale_major in (None, "K"):
         sm = SCALE_K_MAJOR
         _need(tuple(a_scale.shape) == (m, kb), "K-major a_scale must be (%d, %d)" % (m, kb))

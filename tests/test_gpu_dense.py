@@ -154,6 +154,21 @@ def test_layout_equivalence_bit_exact(fp8g):
     assert np.array_equal(bits16(_run(fp8g, wk)), bits16(_run(fp8g, wm)))
 
 
+@pytest.mark.parametrize("major", ["K", "MN"])
+def test_scalar_b_scale_is_the_constant_block_grid(fp8g, major):
+    # the page's b_scale may be a scalar (only a non-scalar tensor must be
+    # contiguous): the same result, bit for bit, as that value on every block
+    w = workloads.dense(300, 640, 768, seed=93, scale_major=major)
+    d = to_device(w)
+    s = torch.tensor([0.03125], dtype=torch.float32, device="cuda")
+    grid = torch.full_like(d["b_scale"], 0.03125)
+    out1 = fp8g.gemm_fp8_nt_groupwise(d["a"], d["b"], d["a_scale"], s, scale_major_mode=major)
+    out2 = fp8g.gemm_fp8_nt_groupwise(d["a"], d["b"], d["a_scale"], grid, scale_major_mode=major)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert out1.float().abs().sum() > 0
+
+
 @pytest.mark.parametrize("mma_sm", [0, 2])
 @pytest.mark.parametrize("mnk", [(333, 640, 512), (4096, 2048, 1024)])
 def test_mma_sm_hint_does_not_change_results(fp8g, mma_sm, mnk):
