@@ -52,6 +52,32 @@ def test_unaligned_total_rows(fp8g, oracle_mod):
     assert_close(as_f64(out)[rows], ref[rows], "grouped unaligned")
 
 
+def test_all_padding_writes_nothing(fp8g):
+    mi = torch.full((256,), -1, dtype=torch.int32)
+    w = workloads.grouped(0, 0, 3, 256, 256, seed=6, m_indices=mi)
+    out = _run(fp8g, w)
+    assert not written_rows(out).any()
+    assert fp8g.get_device_status(clear=True) == 0
+
+
+def test_padding_rows_inside_a_block(fp8g, oracle_mod):
+    # -1 rows between an expert's rows (the block still holds one expert): only
+    # the expert's rows are computed and written
+    mi = torch.full((384,), -1, dtype=torch.int32)
+    mi[0:128:3] = 0
+    mi[128:256:2] = 2
+    mi[300:310] = 1
+    w = workloads.grouped(0, 0, 3, 384, 384, seed=7, m_indices=mi)
+    out = _run(fp8g, w)
+    ref, _, written = oracle_mod.group_gemm_contiguous(w["a"], w["b"], w["a_scale"], w["b_scale"],
+                                                       w["m_indices"])
+    rows = written.any(axis=1)
+    assert np.array_equal(written_rows(out), rows)
+    assert np.array_equal(rows, (mi >= 0).numpy())
+    assert_close(as_f64(out)[rows], ref[rows], "grouped interleaved padding")
+    assert fp8g.get_device_status(clear=True) == 0
+
+
 def test_moe_4096_tokens_top8_64_experts_sampled(fp8g, oracle_mod):
     w = workloads.make("grouped_4096tok_top8_e64_n4096_k7168")
     out = _run(fp8g, w)
