@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -61,6 +62,7 @@ struct DeviceState {
     unsigned int* status = nullptr;
     bool kernel_ready[kNumKernels] = {};
     bool norm_ready = false;
+    int norm_ring_ctas = 0;  // resident CTAs per SM of the ring norm kernel at its largest row
     bool moe_ready = false;
     uint8_t* moe_static_scratch = nullptr;  // address of g_moe_static_scratch on this device
     int resident[kNumKernels] = {};  // CTAs (or CTA pairs) of a persistent grid
@@ -636,14 +638,27 @@ fp8g_status_t fused_add_rmsnorm_fp8_block_quant(void* out, float* block_scale, v
         DeviceState* ds = nullptr;
         fp8g_status_t s = device_state(&ds);
         if (s != FP8G_OK) return s;
-        const size_t smem = static_cast<size_t>(hidden) * 2;
-        auto kernel = fp8g::fused_add_rmsnorm_quant_kernel;
+        // rows of up to NQR_MAX_HIDDEN: the persistent kernel with the bulk-copy
+        // ring; longer rows: one CTA per row
+        const bool ring = hidden <= fp8g::NQR_MAX_HIDDEN;
+        const size_t ring_max_smem =
+            static_cast<size_t>(fp8g::NQR_STAGES) * 4 * fp8g::NQR_MAX_HIDDEN;
         {
             std::lock_guard<std::mutex> lock(g_mutex);
             if (!ds->norm_ready) {
-                cudaError_t e = cudaFuncSetAttribute(
-                    kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 65536 * 2);
-                if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+                cudaError_t e = cudaFuncSetAttribute(fp8g::fused_add_rmsnorm_quant_kernel,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     65536 * 2);
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(fp8g::fused_add_rmsnorm_quant_ring_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(ring_max_smem));
+                if (e == cudaSuccess)
+                    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                        &ds->norm_ring_ctas, fp8g::fused_add_rmsnorm_quant_ring_kernel,
+                        fp8g::NQ_THREADS, ring_max_smem);
+                if (e != cudaSuccess) return cuda_fail(e, "norm kernel attributes");
+                if (ds->norm_ring_ctas < 1) ds->norm_ring_ctas = 1;
                 ds->norm_ready = true;
             }
         }
@@ -651,18 +666,34 @@ fp8g_status_t fused_add_rmsnorm_fp8_block_quant(void* out, float* block_scale, v
         attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr.val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(rows), 1, 1);
         cfg.blockDim = dim3(fp8g::NQ_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
         (void)cudaGetLastError();
-        cudaError_t e = cudaLaunchKernelEx(
-            &cfg, kernel, static_cast<uint8_t*>(out), block_scale, static_cast<uint16_t*>(normed_out),
-            static_cast<const uint16_t*>(input), static_cast<uint16_t*>(residual),
-            static_cast<const uint16_t*>(weight), eps, static_cast<int>(rows),
-            static_cast<int>(hidden));
+        cudaError_t e;
+        if (ring) {
+            const int64_t grid = std::min<int64_t>(rows, int64_t(ds->sm_count) * ds->norm_ring_ctas);
+            cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+            cfg.dynamicSmemBytes = static_cast<size_t>(fp8g::NQR_STAGES) * 4 * hidden;
+            e = cudaLaunchKernelEx(&cfg, fp8g::fused_add_rmsnorm_quant_ring_kernel,
+                                   static_cast<uint8_t*>(out), block_scale,
+                                   static_cast<uint16_t*>(normed_out),
+                                   static_cast<const uint16_t*>(input),
+                                   static_cast<uint16_t*>(residual),
+                                   static_cast<const uint16_t*>(weight), eps,
+                                   static_cast<int>(rows), static_cast<int>(hidden), ds->status);
+        } else {
+            cfg.gridDim = dim3(static_cast<unsigned>(rows), 1, 1);
+            cfg.dynamicSmemBytes = static_cast<size_t>(hidden) * 2;
+            e = cudaLaunchKernelEx(&cfg, fp8g::fused_add_rmsnorm_quant_kernel,
+                                   static_cast<uint8_t*>(out), block_scale,
+                                   static_cast<uint16_t*>(normed_out),
+                                   static_cast<const uint16_t*>(input),
+                                   static_cast<uint16_t*>(residual),
+                                   static_cast<const uint16_t*>(weight), eps,
+                                   static_cast<int>(rows), static_cast<int>(hidden));
+        }
         if (e == cudaSuccess) e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
         t_last_error.clear();
