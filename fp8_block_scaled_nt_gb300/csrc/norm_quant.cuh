@@ -17,7 +17,7 @@
 //
 // Rows of up to 8192 elements run on a persistent kernel that pulls each row
 // with two bulk copies into a two-slot shared-memory ring (below); longer rows
-// run one CTA per row.  One CTA per row: pass 1 streams input and residual with 16-byte loads,
+// run one CTA per row, where pass 1 streams input and residual with 16-byte loads,
 // writes the new residual, keeps x in shared memory and reduces the sum of
 // squares; pass 2 gives each 128-column block to a half-warp (8 values per
 // lane), which normalises, finds the block's amax with four shuffles and
