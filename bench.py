@@ -613,7 +613,7 @@ def run_ours(args):
     peaks, peaks_src = load_peaks()
     kernel_name = {"dense": "gemm_kernel<dense>", "grouped": "gemm_kernel<grouped>",
                    "masked": "gemm_kernel<masked>",
-                   "norm": "fused_add_rmsnorm_quant_kernel", "bmm": "bmm_kernel",
+                   "norm": "fused_add_rmsnorm_quant_ring_kernel", "bmm": "bmm_kernel",
                    "moe": "moe layer (route, quantise, 2 x gemm_kernel<grouped>, SwiGLU, "
                           "combine)"}[kind]
     if bound == "tensor":
