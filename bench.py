@@ -455,10 +455,14 @@ def run_reference(args):
             flops += r * d
     elapsed = sum(times)
     value = flops / elapsed / div
-    what = ("seeded rows per step of %s (add, RMSNorm and 1x128 quantisation of each row in "
-            "FP64)" if workloads.CONFIGS[args.workload]["kind"] == "norm" else
-            "seeded output elements per step of %s (each the full k-long FP64 dot product and "
-            "scale promotion)")
+    kind = workloads.CONFIGS[args.workload]["kind"]
+    what = {"norm": "seeded rows per step of %s (add, RMSNorm and 1x128 quantisation of each "
+                    "row in FP64)",
+            "moe": "seeded tokens per step of %s (the whole layer for each token: quantisation, "
+                   "its experts' fc1, SwiGLU, fc2 and the sum, in FP64)",
+            "bmm": "seeded rows of batch 0 per step of %s (each row's full FP64 products and "
+                   "scales)"}.get(kind, "seeded output elements per step of %s (each the full "
+                                        "k-long FP64 dot product and scale promotion)")
     line = {
         "impl": "reference", "metric": metric, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
