@@ -58,6 +58,8 @@ def _load():
         lib.oracle_quant_1x128.restype = None
         lib.oracle_moe_deepseek_fp8_block_scale.argtypes = [P, P, P, P, P, P, I64, I64, I64,
                                                             I64, I64, P]
+        lib.oracle_moe_swiglu_quant.argtypes = [P, I64, I64, P, P]
+        lib.oracle_moe_combine.argtypes = [P, P, I64, I64, I64, P]
         lib.oracle_e5m2_table.argtypes = [P]
         lib.oracle_e5m2_table.restype = None
         lib.oracle_bmm_fp8.argtypes = [P, P, I, I, P, I, P, I, I64, I64, I64, I64, I, P, P]
@@ -65,6 +67,7 @@ def _load():
                   "oracle_bmm_fp8",
                   "oracle_fused_add_rmsnorm_fp8_block_quant",
                   "oracle_moe_deepseek_fp8_block_scale",
+                  "oracle_moe_swiglu_quant", "oracle_moe_combine",
                   "oracle_group_gemm_contiguous", "oracle_group_gemm_contiguous_at",
                   "oracle_batch_gemm_masked", "oracle_batch_gemm_masked_at",
                   "oracle_num_threads"):
@@ -311,6 +314,38 @@ def moe_deepseek_fp8_block_scale(input_bits, token_selected, w1, w2, s1, s2):
     if rc == -2:
         raise ValueError("moe: token_selected holds an expert id outside [-1, num_experts)")
     _check(rc, "moe_deepseek_fp8_block_scale")
+    return out
+
+
+def moe_swiglu_quant(h_bits):
+    """The MoE layer's SwiGLU step on given fc1 outputs: h (rows, 2*inter) BF16
+    encodings (gate, then up).  act = silu(gate) * up in FP64, then its 1 x 128
+    quantisation; returns (codes uint8 (rows, inter), scales float32 (rows,
+    inter // 128))."""
+    h = _arr(h_bits, np.uint16)
+    rows, two_i = h.shape
+    inter = two_i // 2
+    codes = np.empty((rows, inter), np.uint8)
+    scales = np.empty((rows, inter // 128 if inter % 128 == 0 else 0), np.float32)
+    rc = _load().oracle_moe_swiglu_quant(_p(h), rows, inter, _p(codes), _p(scales))
+    _check(rc, "moe_swiglu_quant")
+    return codes, scales
+
+
+def moe_combine(y_bits, row_of):
+    """The MoE layer's combine step on given fc2 outputs: y (rows, hidden) BF16
+    encodings, row_of (tokens, top_k) int32 rows of y (-1: empty slot).
+    Returns the BF16 encodings of out (tokens, hidden): each token's rows summed
+    exactly and rounded once."""
+    y = _arr(y_bits, np.uint16)
+    ro = _arr(row_of, np.int32)
+    tokens, top_k = ro.shape
+    hidden = y.shape[1]
+    if ro.size and (ro.max() >= y.shape[0]):
+        raise ValueError("row_of points past the rows of y")
+    out = np.empty((tokens, hidden), np.uint16)
+    rc = _load().oracle_moe_combine(_p(y), _p(ro), tokens, top_k, hidden, _p(out))
+    _check(rc, "moe_combine")
     return out
 
 

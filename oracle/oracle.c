@@ -586,6 +586,54 @@ static double block_scaled_dot(const double* dec, const uint8_t* xq, const float
     return r;
 }
 
+/* SwiGLU of one routed row h (BF16 encodings: gate h[0, inter), up
+ * h[inter, 2 inter)), act = silu(gate) * up with silu(g) = g / (1 + e^-g) in
+ * FP64, then its 1 x 128 quantisation. */
+static void swiglu_quant_row(const uint16_t* h, int64_t inter, double* act, uint8_t* codes,
+                             float* scales)
+{
+    for (int64_t j = 0; j < inter; ++j) {
+        const double g = bf16_value(h[j]);
+        act[j] = g / (1.0 + exp(-g)) * bf16_value(h[inter + j]);
+    }
+    quant_row_1x128(act, inter, codes, scales);
+}
+
+int oracle_moe_swiglu_quant(const uint16_t* h, int64_t rows, int64_t inter, uint8_t* codes,
+                            float* scales)
+{
+    if (rows < 0 || inter <= 0 || inter % KBLOCK)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        double* act = (double*)malloc(sizeof(double) * (size_t)inter);
+        swiglu_quant_row(h + r * 2 * inter, inter, act, codes + r * inter,
+                         scales + r * (inter / KBLOCK));
+        free(act);
+    }
+    return 0;
+}
+
+int oracle_moe_combine(const uint16_t* y, const int32_t* row_of, int64_t tokens, int64_t top_k,
+                       int64_t hidden, uint16_t* out)
+{
+    if (tokens < 0 || top_k <= 0 || hidden <= 0)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < tokens; ++t)
+        for (int64_t j = 0; j < hidden; ++j) {
+            /* a sum of BF16 values is exact in FP64 here; one rounding */
+            double acc = 0.0;
+            for (int64_t s = 0; s < top_k; ++s) {
+                const int32_t r = row_of[t * top_k + s];
+                if (r >= 0)
+                    acc += bf16_value(y[(int64_t)r * hidden + j]);
+            }
+            round_one(acc, ORACLE_OUT_BF16, &out[t * hidden + j]);
+        }
+    return 0;
+}
+
 int oracle_moe_deepseek_fp8_block_scale(const uint16_t* input, const int32_t* token_selected,
                                         const uint8_t* w1, const uint8_t* w2,
                                         const float* s1, const float* s2, int64_t num_tokens,
@@ -606,7 +654,7 @@ int oracle_moe_deepseek_fp8_block_scale(const uint16_t* input, const int32_t* to
         double* x = (double*)malloc(sizeof(double) * (size_t)hidden);
         uint8_t* xq = (uint8_t*)malloc((size_t)hidden);
         float* xs = (float*)malloc(sizeof(float) * (size_t)hb);
-        double* h = (double*)malloc(sizeof(double) * (size_t)(2 * inter));
+        uint16_t* h = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(2 * inter));
         double* act = (double*)malloc(sizeof(double) * (size_t)inter);
         uint8_t* aq = (uint8_t*)malloc((size_t)inter);
         float* as = (float*)malloc(sizeof(float) * (size_t)ib);
@@ -624,13 +672,10 @@ int oracle_moe_deepseek_fp8_block_scale(const uint16_t* input, const int32_t* to
             for (int64_t j = 0; j < 2 * inter; ++j) {
                 const uint8_t* wr = w1 + (e * 2 * inter + j) * hidden;
                 const float* sr = s1 + (e * (2 * inter / KBLOCK) + j / KBLOCK) * hb;
-                h[j] = round_one(block_scaled_dot(dec, xq, xs, wr, sr, hidden), ORACLE_OUT_BF16,
-                                 NULL);
+                round_one(block_scaled_dot(dec, xq, xs, wr, sr, hidden), ORACLE_OUT_BF16, &h[j]);
             }
-            /* SwiGLU: silu(gate) * up, silu(g) = g / (1 + e^-g) */
-            for (int64_t j = 0; j < inter; ++j)
-                act[j] = h[j] / (1.0 + exp(-h[j])) * h[inter + j];
-            quant_row_1x128(act, inter, aq, as);
+            /* SwiGLU and its 1 x 128 quantisation */
+            swiglu_quant_row(h, inter, act, aq, as);
             /* fc2 -> BF16, summed over the token's experts */
             for (int64_t j = 0; j < hidden; ++j) {
                 const uint8_t* wr = w2 + (e * hidden + j) * inter;

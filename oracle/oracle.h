@@ -170,6 +170,21 @@ int oracle_moe_deepseek_fp8_block_scale(const uint16_t* input, const int32_t* to
                                         int64_t num_experts, int64_t top_k, int64_t hidden,
                                         int64_t inter, uint16_t* out);
 
+/* The SwiGLU step of the MoE layer above on given fc1 outputs: for each of
+ * `rows` rows of h (BF16 encodings, 2*inter wide: gate, then up),
+ * act = silu(gate) * up in FP64 and its 1x128 quantisation, codes (rows, inter)
+ * and scales (rows, inter/128) -- the same function the layer applies.
+ * Returns -1 unless inter is a positive multiple of 128 and rows >= 0. */
+int oracle_moe_swiglu_quant(const uint16_t* h, int64_t rows, int64_t inter, uint8_t* codes,
+                            float* scales);
+
+/* The combine step of the MoE layer above on given fc2 outputs: out[t] =
+ * BF16(sum over the slots s with row_of[t, s] >= 0 of y[row_of[t, s]]), the
+ * sum exact in FP64 and rounded once; y (rows, hidden) and out (tokens, hidden)
+ * are BF16 encodings, row_of (tokens, top_k). */
+int oracle_moe_combine(const uint16_t* y, const int32_t* row_of, int64_t tokens, int64_t top_k,
+                       int64_t hidden, uint16_t* out);
+
 /* FP8 formats of bmm_fp8's operands. */
 #define ORACLE_FP8_E4M3 0
 #define ORACLE_FP8_E5M2 1

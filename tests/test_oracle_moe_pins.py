@@ -151,3 +151,94 @@ def test_quantiser_agrees_with_the_norm_path(oracle_mod):
     got = oracle_mod.fused_add_rmsnorm_fp8_block_quant(b(inp), b(res), b(w))
     codes, scales = oracle_mod.quant_1x128(f64(got["normed_out"]))
     assert np.array_equal(codes, got["out"]) and np.array_equal(scales, got["block_scale"])
+
+
+# ------------------------------------------------ the layer's steps, one by one
+
+def bf16_bits(x):
+    return torch.tensor(np.asarray(x, np.float32)).bfloat16().view(torch.int16).numpy() \
+        .view(np.uint16)
+
+
+def test_swiglu_step_is_the_layers(oracle_mod):
+    """The SwiGLU step the oracle exposes is the one its layer applies: the
+    layer rebuilt from the pinned grouped GEMM and this step gives the same bits."""
+    x, ts, w1, w2, s1, s2 = random_layer(7, 12, 256, 256, 4, 2)
+    xq, xs = oracle_mod.quant_1x128(f64(x))
+    want = oracle_mod.moe_deepseek_fp8_block_scale(x, ts, w1, w2, s1, s2)
+    out = np.zeros((12, 256))
+    for t in range(12):
+        for s in range(2):
+            e = ts[t, s]
+            if e < 0:
+                continue
+            a = np.zeros((128, 256), np.uint8)
+            sa = np.zeros((128, 2), np.float32)
+            a[0], sa[0] = xq[t], xs[t]
+            mi = np.full(128, -1, np.int32)
+            mi[0] = 0
+            _, hb, _ = oracle_mod.group_gemm_contiguous(a, w1[e:e + 1], sa, s1[e:e + 1], mi)
+            aq, asc = oracle_mod.moe_swiglu_quant(hb[:1])
+            a2 = np.zeros((128, 256), np.uint8)
+            sa2 = np.zeros((128, 2), np.float32)
+            a2[0], sa2[0] = aq[0], asc[0]
+            _, yb, _ = oracle_mod.group_gemm_contiguous(a2, w2[e:e + 1], sa2, s2[e:e + 1], mi)
+            out[t] += f64(yb[0])
+    _, bits = oracle_mod.round_to(out)
+    assert np.array_equal(bits, want)
+
+
+def test_swiglu_step_special_cases(oracle_mod):
+    rng = np.random.default_rng(8)
+    up = rng.normal(size=(3, 256))
+    # a zero gate or a zero up part: act = 0, scale 0 and codes 0
+    h = np.concatenate([np.zeros((3, 256)), up], axis=1)
+    codes, scales = oracle_mod.moe_swiglu_quant(bf16_bits(h))
+    assert not codes.any() and not scales.any()
+    h = np.concatenate([up, np.zeros((3, 256))], axis=1)
+    codes, scales = oracle_mod.moe_swiglu_quant(bf16_bits(h))
+    assert not codes.any() and not scales.any()
+    # gates >= 64: e^-g < 2^-53, so silu(g) = g exactly and the step is the
+    # (separately pinned) 1x128 quantisation of gate * up
+    g = 64.0 * 2.0 ** rng.integers(0, 6, size=(3, 256))
+    hb = bf16_bits(np.concatenate([g, up], axis=1))
+    gq, uq = f64(hb[:, :256]), f64(hb[:, 256:])
+    codes, scales = oracle_mod.moe_swiglu_quant(hb)
+    want_c, want_s = oracle_mod.quant_1x128(gq * uq)
+    assert np.array_equal(codes, want_c) and np.array_equal(scales, want_s)
+    # gates <= -1024: e^-g overflows, silu(g) = -0, nothing survives
+    hb = bf16_bits(np.concatenate([np.full((3, 256), -1024.0), up], axis=1))
+    codes, scales = oracle_mod.moe_swiglu_quant(hb)
+    assert not scales.any() and np.all((codes == 0) | (codes == 0x80))
+
+
+def test_swiglu_step_sign_symmetry(oracle_mod):
+    # negating the up part negates act exactly: same scales, sign bits flipped
+    rng = np.random.default_rng(9)
+    h = bf16_bits(rng.normal(size=(4, 512)) * 3)
+    neg = h.copy()
+    neg[:, 256:] ^= 0x8000
+    c1, s1 = oracle_mod.moe_swiglu_quant(h)
+    c2, s2 = oracle_mod.moe_swiglu_quant(neg)
+    assert np.array_equal(s1, s2)
+    nz = (c1 & 0x7F) != 0
+    assert np.array_equal(c2[nz], c1[nz] ^ 0x80)
+
+
+def test_combine_step_hand_worked_and_invariants(oracle_mod):
+    # hand-worked: 1 + 2^-8 is the midpoint of BF16 1.0 (0x3F80) and 1 + 2^-7
+    # (0x3F81) and rounds to the even 0x3F80; 1 + 3 * 2^-9 lies above it: 0x3F81
+    y = bf16_bits(np.array([[1.0], [2.0 ** -8], [3 * 2.0 ** -9], [-1.0]]))
+    row_of = np.array([[0, 1], [0, 2], [3, -1], [-1, -1], [1, 3]], np.int32)
+    out = oracle_mod.moe_combine(y, row_of)
+    assert out[:, 0].tolist() == [0x3F80, 0x3F81, 0xBF80, 0x0000, 0xBF7F]
+    rng = np.random.default_rng(10)
+    y = bf16_bits(rng.normal(size=(40, 256)))
+    ro = rng.permutation(40)[:32].reshape(8, 4).astype(np.int32)
+    ro[2, 1] = -1
+    base = oracle_mod.moe_combine(y, ro)
+    # one slot: the row itself; a row taken twice: exactly double; any slot order
+    assert np.array_equal(oracle_mod.moe_combine(y, ro[:, :1]), y[ro[:, 0]])
+    twice = oracle_mod.moe_combine(y, np.repeat(ro[:, :1], 2, axis=1))
+    assert np.array_equal(f64(twice), 2 * f64(y[ro[:, 0]]))
+    assert np.array_equal(oracle_mod.moe_combine(y, ro[:, ::-1].copy()), base)
