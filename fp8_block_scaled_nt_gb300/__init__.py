@@ -25,7 +25,8 @@ import ctypes
 import os
 
 __all__ = [
-    "Fp8gError", "load", "last_error", "get_device_status",
+    "Fp8gError", "load", "last_error", "get_device_status", "get_stream_status",
+    "moe_workspace_layout",
     "fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
     "gemm_fp8_nt_groupwise", "group_deepgemm_fp8_nt_groupwise",
     "batch_deepgemm_fp8_nt_groupwise", "fused_add_rmsnorm_fp8_block_quant",
@@ -78,9 +79,15 @@ def load():
                                                        I64, P, ctypes.c_size_t, P]
     lib.fused_moe_deepseek_fp8_block_scale_noalloc.argtypes = [P, P, P, P, P, P, P, I64, I64,
                                                                I64, I64, I64, P]
+    lib.fp8g_get_stream_status.argtypes = [ctypes.POINTER(ctypes.c_uint), I, P]
+    lib.fused_moe_deepseek_fp8_block_scale_workspace_layout.argtypes = [
+        I64, I64, I64, I64, I64, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_size_t)]
+    lib.fp8g_testing_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.fp8g_testing_set_wait_limit_ns.restype = None
     for f in ("fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
               "fused_add_rmsnorm_fp8_block_quant", "fused_moe_deepseek_fp8_block_scale", "bmm_fp8",
-              "fused_moe_deepseek_fp8_block_scale_noalloc", "fp8g_get_device_status"):
+              "fused_moe_deepseek_fp8_block_scale_noalloc", "fp8g_get_device_status",
+              "fp8g_get_stream_status", "fused_moe_deepseek_fp8_block_scale_workspace_layout"):
         getattr(lib, f).restype = ctypes.c_int
     lib.fp8g_last_error.argtypes = []
     lib.fp8g_last_error.restype = ctypes.c_char_p
@@ -104,6 +111,33 @@ def get_device_status(clear=True):
     if rc not in (OK, ERR_TIMEOUT):
         _raise_on(rc, "fp8g_get_device_status")
     return v.value
+
+
+def get_stream_status(clear=True, stream=None):
+    """The same bits, read in the order of ``stream`` (the current stream when
+    omitted): waits for that stream only."""
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    v = ctypes.c_uint(0)
+    rc = load().fp8g_get_stream_status(ctypes.byref(v), 1 if clear else 0, stream.cuda_stream)
+    if rc not in (OK, ERR_TIMEOUT):
+        _raise_on(rc, "fp8g_get_stream_status")
+    return v.value
+
+
+MOE_WORKSPACE_REGIONS = ("m_indices", "row_of", "a1", "a1_scale", "h", "a2", "a2_scale", "y")
+
+
+def moe_workspace_layout(num_tokens, num_experts, top_k, hidden_size, inter_size):
+    """Rows M of the MoE layer's routed layout and the byte offset of each
+    workspace region (``MOE_WORKSPACE_REGIONS``; see include/fp8g.h)."""
+    rows = ctypes.c_int64(0)
+    offs = (ctypes.c_size_t * 8)()
+    rc = load().fused_moe_deepseek_fp8_block_scale_workspace_layout(
+        num_tokens, num_experts, top_k, hidden_size, inter_size, ctypes.byref(rows), offs)
+    _raise_on(rc, "fused_moe_deepseek_fp8_block_scale_workspace_layout")
+    return rows.value, dict(zip(MOE_WORKSPACE_REGIONS, (int(o) for o in offs)))
 
 
 # ------------------------------------------------------------- marshalling
@@ -168,9 +202,13 @@ def _check_granularity(g):
 
 # ------------------------------------------------------------- C entry points
 
-def fp8_gemm_nt_groupwise(a, b, a_scale, b_scale, out, scale_major="K", mma_sm=1,
+def fp8_gemm_nt_groupwise(a, b, a_scale, b_scale, out, scale_major="K", mma_sm=0,
                           scale_granularity_mnk=(1, 128, 128), stream=None, output_scale=None):
     """out (m,n) = a (m,k) @ b (n,k).T with groupwise scales; returns out.
+
+    ``mma_sm``: 0 picks the tile shape (one SM per 128 x 256 tile, or a CTA pair
+    per 256 x 256 tile) from the problem size; 1 and 2 force one or the other.
+    Results are bit-identical either way.
 
     ``out`` is BF16/FP16, or E4M3 (``float8_e4m3fn`` or ``uint8`` codes) together
     with ``output_scale``, a one-element float32 device tensor s: out = E4M3(R / s).
@@ -298,14 +336,10 @@ def moe_workspace_size(num_tokens, num_experts, top_k, hidden_size, inter_size):
         num_tokens, num_experts, top_k, hidden_size, inter_size))
 
 
-def fused_moe_deepseek_fp8_block_scale(input, token_selected, fc1_weights, fc2_weights, out,
-                                       fc1_scales, fc2_scales, workspace=None, stream=None):
-    """DeepSeek FP8 block-scale MoE layer (see include/fp8g.h): out (T, H) BF16 =
-    sum over each token's selected experts of fc2(SwiGLU(fc1(input))).
-
-    ``workspace`` is a uint8 CUDA tensor of at least ``moe_workspace_size(...)``
-    bytes; when omitted one is allocated with torch for this call.
-    """
+def _moe_args(input, token_selected, fc1_weights, fc2_weights, out, fc1_scales, fc2_scales):
+    """Checks the MoE layer's tensors against one another (the C ABI gets only
+    pointers and sizes, so a mismatch must be caught here) and returns
+    (T, E, top_k, H, I, device)."""
     torch = _torch()
     _need(input.dim() == 2 and input.dtype == torch.bfloat16, "input must be bfloat16 (T, H)")
     t, hdim = input.shape
@@ -313,12 +347,11 @@ def fused_moe_deepseek_fp8_block_scale(input, token_selected, fc1_weights, fc2_w
           token_selected.shape[0] == t, "token_selected must be int32 (T, top_k)")
     top_k = token_selected.shape[1]
     _e4m3(fc1_weights, "fc1_weights"), _e4m3(fc2_weights, "fc2_weights")
-    _need(fc1_weights.dim() == 3 and fc1_weights.shape[2] == hdim,
-          "fc1_weights must be (E, 2 I, H)")
+    _need(fc1_weights.dim() == 3 and fc1_weights.shape[2] == hdim and
+          fc1_weights.shape[1] % 2 == 0, "fc1_weights must be (E, 2 I, H)")
     e, two_i = fc1_weights.shape[0], fc1_weights.shape[1]
     inter = two_i // 2
-    _need(two_i % 2 == 0 and tuple(fc2_weights.shape) == (e, hdim, inter),
-          "fc2_weights must be (E, H, I)")
+    _need(tuple(fc2_weights.shape) == (e, hdim, inter), "fc2_weights must be (E, H, I)")
     _need(fc1_scales.dtype == torch.float32 and
           tuple(fc1_scales.shape) == (e, two_i // 128, hdim // 128),
           "fc1_scales must be float32 (E, 2 I / 128, H / 128)")
@@ -330,6 +363,20 @@ def fused_moe_deepseek_fp8_block_scale(input, token_selected, fc1_weights, fc2_w
     dev = _cuda_contig((input, token_selected, fc1_weights, fc2_weights, out, fc1_scales,
                         fc2_scales), ("input", "token_selected", "fc1_weights", "fc2_weights",
                                       "out", "fc1_scales", "fc2_scales"))
+    return t, e, top_k, hdim, inter, dev
+
+
+def fused_moe_deepseek_fp8_block_scale(input, token_selected, fc1_weights, fc2_weights, out,
+                                       fc1_scales, fc2_scales, workspace=None, stream=None):
+    """DeepSeek FP8 block-scale MoE layer (see include/fp8g.h): out (T, H) BF16 =
+    sum over each token's selected experts of fc2(SwiGLU(fc1(input))).
+
+    ``workspace`` is a uint8 CUDA tensor of at least ``moe_workspace_size(...)``
+    bytes; when omitted one is allocated with torch for this call.
+    """
+    torch = _torch()
+    t, e, top_k, hdim, inter, dev = _moe_args(input, token_selected, fc1_weights, fc2_weights,
+                                              out, fc1_scales, fc2_scales)
     need = moe_workspace_size(t, e, top_k, hdim, inter)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
@@ -344,21 +391,16 @@ def fused_moe_deepseek_fp8_block_scale(input, token_selected, fc1_weights, fc2_w
 
 def fused_moe_deepseek_fp8_block_scale_noalloc(input, token_selected, fc1_weights, fc2_weights,
                                                out, fc1_scales, fc2_scales, stream=None):
-    """The MoE layer with its scratch in the library's fixed per-device array
-    (MOE_STATIC_SCRATCH_BYTES); nothing is allocated.  Calls that can overlap on
-    one device race on that scratch."""
-    torch = _torch()
-    t, hdim = input.shape
-    top_k = token_selected.shape[1]
-    e, two_i = fc1_weights.shape[0], fc1_weights.shape[1]
-    _need(input.dtype == torch.bfloat16 and out.dtype == torch.bfloat16 and
-          token_selected.dtype == torch.int32, "input/out bfloat16, token_selected int32")
-    dev = _cuda_contig((input, token_selected, fc1_weights, fc2_weights, out, fc1_scales,
-                        fc2_scales), ("input", "token_selected", "fc1_weights", "fc2_weights",
-                                      "out", "fc1_scales", "fc2_scales"))
+    """The MoE layer for callers that cannot hand the library device memory (a
+    host that reserved all of it for its own pool, a serving loop that must not
+    call cudaMalloc): its scratch is the library's fixed per-device array of
+    MOE_STATIC_SCRATCH_BYTES and nothing is allocated.  Same checks as the
+    workspace form; calls that can overlap on one device race on that array."""
+    t, e, top_k, hdim, inter, dev = _moe_args(input, token_selected, fc1_weights, fc2_weights,
+                                              out, fc1_scales, fc2_scales)
     rc = load().fused_moe_deepseek_fp8_block_scale_noalloc(
         _ptr(input), _ptr(token_selected), _ptr(fc1_weights), _ptr(fc2_weights), _ptr(out),
-        _ptr(fc1_scales), _ptr(fc2_scales), t, e, top_k, hdim, two_i // 2,
+        _ptr(fc1_scales), _ptr(fc2_scales), t, e, top_k, hdim, inter,
         _stream_handle(stream, dev))
     _raise_on(rc, "fused_moe_deepseek_fp8_block_scale_noalloc")
     return out
@@ -402,10 +444,16 @@ def bmm_fp8(A, B, A_scale, B_scale, dtype=None, out=None, backend="auto", stream
 
 # ------------------------------------------------------------- page signatures
 
-def gemm_fp8_nt_groupwise(a, b, a_scale, b_scale, scale_major_mode=None, mma_sm=1,
+def gemm_fp8_nt_groupwise(a, b, a_scale, b_scale, scale_major_mode=None, mma_sm=None,
                           scale_granularity_mnk=(1, 128, 128), out=None, out_dtype=None,
                           backend="auto", output_scale=None):
-    """The page's ``gemm_fp8_nt_groupwise``: returns out (m, n)."""
+    """The page's ``gemm_fp8_nt_groupwise``: returns out (m, n).
+
+    ``mma_sm``: the page's default (1) configures MATE's MUSA kernels; on GB300
+    it is a hint, and leaving it out picks the tile shape from the problem size
+    (CTA pairs on large problems).  An explicit 1 or 2 forces one SM or a CTA
+    pair per tile.  Results are bit-identical either way.
+    """
     torch = _torch()
     if backend != "auto":
         raise Fp8gError(ERR_UNSUPPORTED, "gemm_fp8_nt_groupwise",
@@ -415,8 +463,9 @@ def gemm_fp8_nt_groupwise(a, b, a_scale, b_scale, scale_major_mode=None, mma_sm=
         default = torch.float8_e4m3fn if output_scale is not None else torch.bfloat16
         out = torch.empty((a.shape[0], b.shape[0]), device=a.device,
                           dtype=out_dtype if out_dtype is not None else default)
-    return fp8_gemm_nt_groupwise(a, b, a_scale, b_scale, out, scale_major_mode or "K", mma_sm,
-                                 scale_granularity_mnk, output_scale=output_scale)
+    return fp8_gemm_nt_groupwise(a, b, a_scale, b_scale, out, scale_major_mode or "K",
+                                 0 if mma_sm is None else mma_sm, scale_granularity_mnk,
+                                 output_scale=output_scale)
 
 
 def group_deepgemm_fp8_nt_groupwise(a, b, a_scale, b_scale, m_indices,

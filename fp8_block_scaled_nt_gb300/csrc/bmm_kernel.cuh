@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-    const Ctl ctl{abort_flag, 0u, p.status};
+    const Ctl ctl{abort_flag, 0u, p.status, p.wait_limit_ns};
     grid_dependency_wait();
     grid_launch_dependents();
 

@@ -19,6 +19,7 @@
 #include <string>
 
 #include "fp8g.h"
+#include "fp8g_testing.h"
 #include "bmm_kernel.cuh"
 #include "gemm_kernel.cuh"
 #include "moe.cuh"
@@ -34,6 +35,10 @@ __device__ unsigned int g_device_status;  // OR of FP8G_DEVICE_* bits, per devic
 static __device__ __align__(256) uint8_t g_moe_static_scratch[FP8G_MOE_STATIC_SCRATCH_BYTES];
 
 thread_local std::string t_last_error;
+
+// Bound of every pipeline wait of the kernels this thread launches (tests of
+// the timeout path shorten it through fp8g_testing_set_wait_limit_ns).
+thread_local uint64_t t_wait_limit_ns = fp8g::WAIT_LIMIT_NS;
 
 fp8g_status_t fail(fp8g_status_t s, const char* fmt, ...) {
     char buf[512];
@@ -113,22 +118,79 @@ fp8g_status_t device_state(DeviceState** out) {
     return FP8G_OK;
 }
 
+// Encoded tensor maps, reused across calls.  A map depends only on the
+// arguments of cuTensorMapEncodeTiled below, so an entry with the same key is
+// the same map whatever happened to the memory in between.  Direct-mapped on a
+// hash of the key; a collision replaces the entry.
+struct MapKey {
+    const void* base;
+    cuuint64_t dims[2];
+    cuuint64_t stride;
+    cuuint32_t box[2];
+    int dtype, l2;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && dims[0] == o.dims[0] && dims[1] == o.dims[1] &&
+               stride == o.stride && box[0] == o.box[0] && box[1] == o.box[1] &&
+               dtype == o.dtype && l2 == o.l2;
+    }
+};
+
+constexpr int kMapCacheSlots = 256;
+struct MapCacheEntry {
+    bool used = false;
+    MapKey key{};
+    CUtensorMap map{};
+};
+std::mutex g_map_mutex;
+MapCacheEntry g_map_cache[kMapCacheSlots];
+
+size_t map_key_hash(const MapKey& k) {
+    uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
+    const uint64_t parts[7] = {k.dims[0], k.dims[1], k.stride, k.box[0], k.box[1],
+                               static_cast<uint64_t>(k.dtype), static_cast<uint64_t>(k.l2)};
+    for (uint64_t v : parts) h = (h ^ v) * 0x100000001B3ull;
+    return static_cast<size_t>(h ^ (h >> 29)) % kMapCacheSlots;
+}
+
+// 2-D tiled map with 128-byte swizzle: `dims` = {inner, outer} elements,
+// `stride` = bytes between outer rows, `box` = {inner, outer} elements.
+fp8g_status_t encode_2d(CUtensorMap* map, const void* base, const cuuint64_t dims[2],
+                        cuuint64_t stride, const cuuint32_t box[2], CUtensorMapDataType dtype,
+                        CUtensorMapL2promotion l2, const char* what) {
+    MapKey key{base, {dims[0], dims[1]}, stride, {box[0], box[1]}, static_cast<int>(dtype),
+               static_cast<int>(l2)};
+    const size_t slot = map_key_hash(key);
+    {
+        std::lock_guard<std::mutex> lock(g_map_mutex);
+        if (g_map_cache[slot].used && g_map_cache[slot].key == key) {
+            *map = g_map_cache[slot].map;
+            return FP8G_OK;
+        }
+    }
+    cuuint64_t strides[1] = {stride};
+    cuuint32_t elem_strides[2] = {1, 1};
+    CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box,
+                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FP8G_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what,
+                    static_cast<int>(r));
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    g_map_cache[slot].used = true;
+    g_map_cache[slot].key = key;
+    g_map_cache[slot].map = *map;
+    return FP8G_OK;
+}
+
 // Row-major E4M3 matrix of `rows` x `k` bytes as a 2-D TMA view, tile
 // `box_rows` x 128 bytes, 128-byte swizzle; rows past the end read as zero.
 fp8g_status_t encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k,
                          int box_rows, const char* what) {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(k)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(fp8g::BLOCK_K), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t elem_strides[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
-                          strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-        return fail(FP8G_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what,
-                    static_cast<int>(r));
-    return FP8G_OK;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(fp8g::BLOCK_K),
+                               static_cast<cuuint32_t>(box_rows)};
+    return encode_2d(map, base, dims, static_cast<cuuint64_t>(k), box,
+                     CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, what);
 }
 
 // Row-major output of `rows` x `n` elements of `esz` bytes as a 2-D TMA view for
@@ -136,18 +198,12 @@ fp8g_status_t encode_map(CUtensorMap* map, const void* base, int64_t rows, int64
 // layout of the kernel's staging).
 fp8g_status_t encode_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t n, int esz,
                              int box_rows) {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(n * esz)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t elem_strides[2] = {1, 1};
-    CUresult r = g_encode(map, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                          2, base, dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-        return fail(FP8G_ERR_CUDA, "cuTensorMapEncodeTiled(out) failed with CUresult %d",
-                    static_cast<int>(r));
-    return FP8G_OK;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(rows)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz),
+                               static_cast<cuuint32_t>(box_rows)};
+    return encode_2d(map, base, dims, static_cast<cuuint64_t>(n * esz), box,
+                     esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, "out");
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -267,6 +323,7 @@ Params base_params(const float* a_scale, const float* b_scale, void* out, int64_
     p.n_tiles = static_cast<int>((n + fp8g::BLOCK_N - 1) / fp8g::BLOCK_N);
     p.m_blocks = static_cast<int>((rows + tile_m - 1) / tile_m);
     p.band_m = 8;
+    p.wait_limit_ns = t_wait_limit_ns;
     return p;
 }
 
@@ -848,6 +905,51 @@ fp8g_status_t fused_moe_deepseek_fp8_block_scale_noalloc(
     } catch (...) {
         return fail(FP8G_ERR_CUDA, "unexpected exception");
     }
+}
+
+fp8g_status_t fused_moe_deepseek_fp8_block_scale_workspace_layout(
+    int64_t num_tokens, int64_t num_experts, int64_t top_k, int64_t hidden_size,
+    int64_t inter_size, int64_t* rows, size_t offsets[8]) {
+    try {
+        if (!rows || !offsets) return fail(FP8G_ERR_INVALID_ARGUMENT, "null pointer argument");
+        fp8g_status_t s = check_moe_shape(num_tokens, num_experts, top_k, hidden_size,
+                                          inter_size);
+        if (s != FP8G_OK) return s;
+        const MoeWorkspace w =
+            moe_workspace(num_tokens, num_experts, top_k, hidden_size, inter_size);
+        *rows = w.rows;
+        const size_t at[8] = {w.m_indices, w.row_of, w.a1, w.a1_scale, w.h, w.a2, w.a2_scale, w.y};
+        for (int i = 0; i < 8; ++i) offsets[i] = at[i];
+        t_last_error.clear();
+        return FP8G_OK;
+    } catch (...) {
+        return fail(FP8G_ERR_CUDA, "unexpected exception");
+    }
+}
+
+fp8g_status_t fp8g_get_stream_status(unsigned int* flags, int clear, cudaStream_t stream) {
+    try {
+        if (!flags) return fail(FP8G_ERR_INVALID_ARGUMENT, "flags is null");
+        DeviceState* ds = nullptr;
+        fp8g_status_t s = device_state(&ds);
+        if (s != FP8G_OK) return s;
+        unsigned int v = 0;
+        cudaError_t e = cudaMemcpyAsync(&v, ds->status, sizeof(v), cudaMemcpyDeviceToHost, stream);
+        if (e == cudaSuccess && clear) e = cudaMemsetAsync(ds->status, 0, sizeof(v), stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+        if (e != cudaSuccess) return cuda_fail(e, "reading the device status word on the stream");
+        *flags = v;
+        if (v & FP8G_DEVICE_TIMEOUT)
+            return fail(FP8G_ERR_TIMEOUT, "a kernel gave up waiting on its pipeline (timeout)");
+        t_last_error.clear();
+        return FP8G_OK;
+    } catch (...) {
+        return fail(FP8G_ERR_CUDA, "unexpected exception");
+    }
+}
+
+void fp8g_testing_set_wait_limit_ns(uint64_t ns) {
+    t_wait_limit_ns = ns ? ns : fp8g::WAIT_LIMIT_NS;
 }
 
 fp8g_status_t fp8g_get_device_status(unsigned int* flags, int clear) {

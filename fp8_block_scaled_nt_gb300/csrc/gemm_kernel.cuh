@@ -85,7 +85,7 @@ constexpr int OUT_STAGE_BYTES = BLOCK_M * OUT_COLS * 2;  // 16 KB per warpgroup
 // one 128-column slice for E4M3).
 constexpr int TILE_STAGE_BYTES = BLOCK_M * 128 * 2;  // 32 KB per warpgroup
 constexpr int STAGE_SLICE_BYTES = BLOCK_M * 128;     // one slice of 128-byte rows
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s: far beyond any legitimate wait
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s default: far beyond any legitimate wait
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
 constexpr uint64_t ABORT_GRACE_NS = 5000000ull;  // 5 ms
 
@@ -137,6 +137,7 @@ struct Params {
     int batch;
     int a_channelwise, b_channelwise;  // scales per row of A / column of B, else one value
     uint32_t idesc;                    // instruction descriptor (operand formats)
+    uint64_t wait_limit_ns;            // bound of every pipeline wait (WAIT_LIMIT_NS by default)
 };
 
 // One output tile as every role of one CTA sees it.
@@ -261,6 +262,7 @@ struct Ctl {
     volatile int* abort_flag;  // this CTA's
     uint32_t peer_abort;       // the other CTA's flag in the cluster window (pairs), else 0
     unsigned int* status;
+    uint64_t limit_ns;         // give up a wait after this long
 };
 
 // Wait for the phase of `bar` with the given parity; false if the CTA aborted
@@ -275,7 +277,7 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, const
         if (mbar_try_wait(bar, parity)) return true;
         if ((spin & 31u) == 0) {
             if (*c.abort_flag) return false;
-            if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            if (global_timer_ns() - t0 > c.limit_ns) {
                 *c.abort_flag = 1;
                 if (c.peer_abort) st_shared_remote(c.peer_abort, 1u);
                 atomicOr(c.status, FP8G_DEVICE_TIMEOUT);
@@ -763,7 +765,12 @@ __device__ __forceinline__ void run_promotion(const Params& p, int rank, uint64_
 
         const RowScales rs = row_scales<FORM>(p, tile, r, quarter, half);
         const bool col_ok = rs.col_ok, row_ok = rs.row_ok;
-        const float *sa = rs.sa, *sb = rs.sb;
+        // A warp none of whose 32 rows is stored (the tail of a masked group or
+        // of an expert's segment, rows past m) or whose half of the tile has no
+        // columns reads nothing from TMEM: it only keeps step with the buffer
+        // hand-offs, which leaves the tensor-memory bandwidth to the live warps.
+        const bool live = col_ok && __any_sync(0xffffffffu, row_ok);
+        const float *sa = live ? rs.sa : nullptr, *sb = live ? rs.sb : nullptr;
         const int sa_step = rs.sa_step, sb_step = rs.sb_step;
 
         uint64_t acc[64];  // FP32 running sums, two columns per register pair
@@ -785,6 +792,20 @@ __device__ __forceinline__ void run_promotion(const Params& p, int rank, uint64_
                 break;
             }
             tc_fence_after_sync();
+            if (!live) {
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (PAIR)
+                        mbar_arrive_remote(buf == 0 ? release0 : release1);
+                    else
+                        mbar_arrive(acc_empty + buf);
+                }
+                if (++buf == 2) {
+                    buf = 0;
+                    bphase ^= 1u;
+                }
+                continue;
+            }
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(buf * BLOCK_N + half * 128);
             const uint64_t s2 = splat2(s);
@@ -930,7 +951,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-    const Ctl ctl{abort_flag, PAIR ? mapa_shared(abort_flag, rank ^ 1) : 0u, p.status};
+    const Ctl ctl{abort_flag, PAIR ? mapa_shared(abort_flag, rank ^ 1) : 0u, p.status,
+                  p.wait_limit_ns};
     // Everything above touches only this CTA's own resources, so it may overlap
     // the tail of the previous kernel on the stream (launched with programmatic
     // stream serialization); global memory is read and written only after it.

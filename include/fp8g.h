@@ -250,19 +250,29 @@ fp8g_status_t fused_moe_deepseek_fp8_block_scale(
     int64_t inter_size, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * The MoE layer above without a caller workspace: the same computation, with its
- * scratch in a fixed array of FP8G_MOE_STATIC_SCRATCH_BYTES per device that the
- * library defines statically (no allocation at call time, by the library or
- * anyone else).  The pages have no counterpart of this call; it serves callers
- * that cannot provide device memory.
+ * The MoE layer above without a caller workspace.  The pages have no
+ * counterpart of this call.  It is for callers that have no way to give the
+ * library device memory: a host program that hands all of the GPU's memory to
+ * its own pool at start-up and offers a plug-in no allocator, or a serving loop
+ * that must never call cudaMalloc because that call can wait for the whole
+ * device and stall every stream.  Such a caller still passes its inputs and
+ * output; the layer's scratch lives in a fixed array of
+ * FP8G_MOE_STATIC_SCRATCH_BYTES that the library defines statically, and the
+ * call allocates nothing (no cudaMalloc, no cudaFree, no allocating library).
  *
+ *   - Cost: every device on which the library's kernels are loaded holds this
+ *     array from then until the process exits, whether or not the call is used.
+ *   - Set-up: the first call on a device looks the array's device address up
+ *     (a host-side query, once per device, under a lock).  Make that first call
+ *     on each device before any stream capture begins.
  *   - Problems whose scratch (fused_moe_deepseek_fp8_block_scale_workspace_size)
  *     exceeds FP8G_MOE_STATIC_SCRATCH_BYTES return FP8G_ERR_UNSUPPORTED with a
  *     message giving both sizes; nothing is launched.
  *   - Nothing in the scratch has to start at zero: the routing step writes every
  *     entry of the layout it reads back, and every other region is written
- *     before it is read within the same call.
- *   - There is one scratch per device: calls that may run at the same time on
+ *     before it is read within the same call.  The array keeps the last call's
+ *     intermediates (layout as in ..._workspace_layout).
+ *   - There is one array per device: calls that may run at the same time on
  *     one device (different streams, or host threads) race on it and corrupt
  *     each other's results.  Calls in one stream are ordered and safe.
  */
@@ -272,6 +282,28 @@ fp8g_status_t fused_moe_deepseek_fp8_block_scale_noalloc(
     const void* fc2_weights, void* out, const float* fc1_scales, const float* fc2_scales,
     int64_t num_tokens, int64_t num_experts, int64_t top_k, int64_t hidden_size,
     int64_t inter_size, cudaStream_t stream);
+
+/*
+ * Layout of the MoE layer's workspace (the same layout sits in the static
+ * scratch of the allocation-free entry point).  Writes the number of rows M of
+ * the routed layout to *rows and the byte offsets of its eight regions, each
+ * 256-byte aligned, to offsets[0..7]:
+ *   0 m_indices  int32 (M)              expert of each routed row, -1 = padding
+ *   1 row_of     int32 (T, K)           routed row of each slot, -1 = empty slot
+ *   2 a1         E4M3 (M, H)            quantised input rows
+ *   3 a1_scale   FP32 (M, H / 128)      their 1x128 scales
+ *   4 h          BF16 (M, 2 I)          fc1 output (gate, then up)
+ *   5 a2         E4M3 (M, I)            quantised SwiGLU activations
+ *   6 a2_scale   FP32 (M, I / 128)      their 1x128 scales
+ *   7 y          BF16 (M, H)            fc2 output
+ * with M = round_up(T * K + 127 * E, 128).  After a call, the regions hold that
+ * call's intermediates on the rows m_indices marks as routed (other rows are
+ * unspecified); the row order inside an expert's segment may differ from call
+ * to call.  Same argument checks as the workspace size query.
+ */
+fp8g_status_t fused_moe_deepseek_fp8_block_scale_workspace_layout(
+    int64_t num_tokens, int64_t num_experts, int64_t top_k, int64_t hidden_size,
+    int64_t inter_size, int64_t* rows, size_t offsets[8]);
 
 /* Message of the last failed call on this thread ("" if none); valid until the
  * thread's next call into the library. */
@@ -285,6 +317,16 @@ const char* fp8g_last_error(void);
  * are reported through *flags only).
  */
 fp8g_status_t fp8g_get_device_status(unsigned int* flags, int clear);
+
+/*
+ * The same word, read in the order of `stream`: waits for the work enqueued on
+ * `stream` so far (and only that stream), copies the word to *flags and, if
+ * `clear` is non-zero, resets it, both as steps of the stream.  The word is
+ * shared by every stream of the device, so it also holds bits that kernels on
+ * other streams have raised by then.  Same return values as
+ * fp8g_get_device_status.
+ */
+fp8g_status_t fp8g_get_stream_status(unsigned int* flags, int clear, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -1,6 +1,6 @@
 """The C-ABI library on a host without a GPU: it loads, exports every entry
-point that include/fp8g.h declares, and rejects bad arguments on the host with
-the documented status codes, before any CUDA call."""
+point that the headers in include/ declare, and rejects bad arguments on the
+host with the documented status codes, before any CUDA call."""
 import ctypes
 import os
 import re
@@ -9,6 +9,8 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "fp8g.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -19,16 +21,20 @@ def lib():
     return fp8g
 
 
-def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+def declared_functions(headers=HEADERS):
+    names = set()
+    for h in headers:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_three_forms_and_helpers():
     names = declared_functions()
     for f in ("fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
-              "fused_add_rmsnorm_fp8_block_quant", "fp8g_last_error", "fp8g_get_device_status"):
+              "fused_add_rmsnorm_fp8_block_quant", "fp8g_last_error", "fp8g_get_device_status",
+              "fp8g_get_stream_status", "fused_moe_deepseek_fp8_block_scale_workspace_layout",
+              "fp8g_testing_set_wait_limit_ns"):
         assert f in names
 
 
@@ -43,7 +49,8 @@ def test_header_compiles_as_c():
     import tempfile
     from fp8_block_scaled_nt_gb300 import _build
     inc = os.path.join(_build.cuda_home(), "include")
-    src = '#include "fp8g.h"\nint main(void){ return (int)FP8G_OK; }\n'
+    src = ('#include "fp8g.h"\n#include "fp8g_testing.h"\n'
+           'int main(void){ return (int)FP8G_OK; }\n')
     with tempfile.TemporaryDirectory() as d:
         p = os.path.join(d, "t.c")
         open(p, "w").write(src)
@@ -200,3 +207,84 @@ def test_binding_rejects_bad_tensors_before_the_library(lib):
                                   torch.empty((128, 256), dtype=torch.bfloat16))
     with pytest.raises(lib.Fp8gError):
         lib.gemm_fp8_nt_groupwise(a8, a8, None, None, backend="mudnn")
+
+
+def test_moe_workspace_layout_matches_the_size(lib):
+    t, e, k, hd, it = 37, 5, 3, 384, 256
+    rows, offs = lib.moe_workspace_layout(t, e, k, hd, it)
+    assert rows == (t * k + 127 * e + 127) // 128 * 128
+    sizes = dict(m_indices=4 * rows, row_of=4 * t * k, a1=rows * hd, a1_scale=4 * rows * hd // 128,
+                 h=2 * rows * 2 * it, a2=rows * it, a2_scale=4 * rows * it // 128, y=2 * rows * hd)
+    at = 0
+    for name in lib.MOE_WORKSPACE_REGIONS:  # in order, each 256-byte aligned, no overlap
+        assert offs[name] == at and at % 256 == 0, name
+        at += (sizes[name] + 255) // 256 * 256
+    assert at == lib.moe_workspace_size(t, e, k, hd, it)
+    with pytest.raises(lib.Fp8gError):
+        lib.moe_workspace_layout(t, e, k, 200, it)
+
+
+def test_stream_status_without_a_device_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host has a GPU")
+    flags = ctypes.c_uint(0)
+    assert lib.load().fp8g_get_stream_status(ctypes.byref(flags), 1, None) == 4
+
+
+def _moe_tensors(t=8, k=2, e=4, hd=256, it=128):
+    import torch
+    return dict(input=torch.zeros((t, hd), dtype=torch.bfloat16),
+                token_selected=torch.zeros((t, k), dtype=torch.int32),
+                fc1_weights=torch.zeros((e, 2 * it, hd), dtype=torch.uint8),
+                fc2_weights=torch.zeros((e, hd, it), dtype=torch.uint8),
+                out=torch.zeros((t, hd), dtype=torch.bfloat16),
+                fc1_scales=torch.ones((e, 2 * it // 128, hd // 128)),
+                fc2_scales=torch.ones((e, hd // 128, it // 128)))
+
+
+@pytest.mark.parametrize("entry", ["fused_moe_deepseek_fp8_block_scale",
+                                   "fused_moe_deepseek_fp8_block_scale_noalloc"])
+@pytest.mark.parametrize("bad,msg", [
+    (dict(out=((4, 256), "bfloat16")), "out must be"),
+    (dict(fc2_weights=((4, 256, 64), "uint8")), "fc2_weights"),
+    (dict(fc1_scales=((4, 1, 2), "float32")), "fc1_scales"),
+    (dict(fc2_scales=((4, 2, 1), "float64")), "fc2_scales"),
+    (dict(token_selected=((7, 2), "int32")), "token_selected"),
+    (dict(fc1_weights=((4, 255, 256), "uint8")), "fc1_weights"),
+])
+def test_moe_wrappers_reject_mismatched_tensors_before_the_library(lib, entry, bad, msg):
+    """Both MoE wrappers check every tensor against the others: the C ABI gets
+    only pointers and sizes, so a smaller out or weight tensor would otherwise
+    be read or written past its end on the device."""
+    import torch
+    args = _moe_tensors()
+    for name, (shape, dt) in bad.items():
+        args[name] = torch.zeros(shape, dtype=getattr(torch, dt))
+    with pytest.raises(ValueError) as e:
+        getattr(lib, entry)(**args)
+    assert msg in str(e.value)
+
+
+def test_page_wrapper_leaves_the_tile_shape_to_the_library(lib, monkeypatch):
+    """The page's gemm_fp8_nt_groupwise defaults mma_sm to MATE's 1; here an
+    omitted mma_sm reaches the C ABI as 0 (automatic: CTA pairs on large
+    problems), and an explicit value goes through unchanged."""
+    import torch
+    seen = []
+
+    class FakeLib:
+        def fp8_gemm_nt_groupwise(self, *args):
+            seen.append(args[14])
+            return 0
+
+    monkeypatch.setattr(lib, "load", lambda: FakeLib())
+    monkeypatch.setattr(lib, "_cuda_contig", lambda ts, names: torch.device("cpu"))
+    monkeypatch.setattr(lib, "_stream_handle", lambda stream, dev: None)
+    a = torch.zeros((256, 256), dtype=torch.uint8)
+    sa, sb = torch.ones((256, 2)), torch.ones((2, 2))
+    lib.gemm_fp8_nt_groupwise(a, a, sa, sb)
+    lib.gemm_fp8_nt_groupwise(a, a, sa, sb, mma_sm=1)
+    lib.gemm_fp8_nt_groupwise(a, a, sa, sb, mma_sm=2)
+    lib.fp8_gemm_nt_groupwise(a, a, sa, sb, torch.empty((256, 256), dtype=torch.bfloat16))
+    assert seen == [0, 1, 2, 0]

@@ -67,6 +67,26 @@ def test_moe_decode_32_groups_sampled_and_expected_m_invariance(fp8g, oracle_mod
         assert np.array_equal(other[rows_expected], base[rows_expected])
 
 
+def test_decode_shape_full_parity_and_expected_m_invariance(fp8g, oracle_mod):
+    # a few tokens per expert in 256-row buffers: every valid row checked, and
+    # the expected_m hint (which picks the kernel's variant) changes no bit
+    w = workloads.make("masked_g32_maxm256_n4096_k7168_decode")
+    out = _run(fp8g, w)
+    mm = w["masked_m"].numpy()
+    rows_expected = np.arange(w["max_m"])[None, :] < mm[:, None]
+    assert np.array_equal(written_rows(out), rows_expected)
+    ref, _, written = oracle_mod.batch_gemm_masked(w["a"], w["b"], w["a_scale"], w["b_scale"],
+                                                   w["masked_m"])
+    assert np.array_equal(written.any(axis=2), rows_expected)
+    assert_close(as_f64(out)[rows_expected], ref[rows_expected], "masked decode")
+    base = bits16(out)
+    for em in (0, 1, 64, 128, 256):
+        again = _run(fp8g, w, expected_m=em)
+        assert np.array_equal(written_rows(again), rows_expected), em
+        assert np.array_equal(bits16(again)[rows_expected], base[rows_expected]), em
+    assert fp8g.get_device_status() == 0
+
+
 def test_all_groups_empty(fp8g):
     mm = torch.zeros(4, dtype=torch.int32)
     w = workloads.masked(4, 128, 256, 256, seed=9, masked_m=mm)

@@ -73,3 +73,11 @@ def test_sample_positions_cover_extra_rows():
     assert r.numel() == 50 + 2 * 256
     assert torch.equal(c[-256:], torch.arange(256))
     assert r.max() < 100 and c.max() < 256
+
+
+def test_masked_decode_config():
+    w = workloads.make("masked_g32_maxm256_n4096_k7168_decode")
+    mm = w["masked_m"]
+    assert mm.dtype == torch.int32 and mm.shape == (32,)
+    assert int(mm.min()) >= 0 and int(mm.max()) <= 16 and w["expected_m"] == 8
+    assert w["a"].shape == (32, 256, 7168) and w["b"].shape == (32, 4096, 7168)

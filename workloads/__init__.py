@@ -27,8 +27,10 @@ NBLOCK = 128  # scale granularity along n
 CONFIGS = {
     "dense_128x256x256": dict(kind="dense", m=128, n=256, k=256, dist="uniform4",
                               scale_exp=(-4.0, 2.0), out_dtype="bf16", seed=1001),
+    # run once with K-major and once with MN-major scales
     "dense_4096x7168x2048": dict(kind="dense", m=4096, n=7168, k=2048, dist="normal",
-                                 scale_exp=(-6.0, 0.0), out_dtype="bf16", seed=1002),
+                                 scale_exp=(-6.0, 0.0), out_dtype="bf16", seed=1002,
+                                 scale_layouts=("K", "MN")),
     # the same GEMM with FP8 (E4M3) output and a per-tensor output scale; with
     # these inputs R has an RMS near 5.4, so R / s (RMS ~87) spans the E4M3
     # range and under 0.1% of the outputs saturate
@@ -41,6 +43,11 @@ CONFIGS = {
     "masked_g32_maxm256_n4096_k7168": dict(
         kind="masked", num_groups=32, max_m=256, n=4096, k=7168, expected_m=128,
         scale_exp=(-6.0, 0.0), seed=1004),
+    # the masked form at decode: a few tokens per expert (masked_m ~ U{0..16},
+    # expected_m 8) in buffers of 256 rows; bound by streaming the weights
+    "masked_g32_maxm256_n4096_k7168_decode": dict(
+        kind="masked", num_groups=32, max_m=256, n=4096, k=7168, expected_m=8, masked_hi=16,
+        scale_exp=(-6.0, 0.0), seed=1010),
     "dense_16384x18432x7168": dict(kind="dense", m=16384, n=18432, k=7168, dist="normal",
                                    scale_exp=(-6.0, 0.0), out_dtype="f16", seed=1005),
     # the producer of the GEMM's activations: 4096 tokens of hidden size 7168
@@ -157,11 +164,13 @@ def grouped(num_tokens, top_k, num_experts, n, k, seed, scale_exp=(-6.0, 0.0),
 
 
 def masked(num_groups, max_m, n, k, seed, scale_exp=(-6.0, 0.0), expected_m=None,
-           device="cpu", masked_m=None, **_):
-    """Masked batched MoE operands; masked_m ~ U{0..max_m} unless given."""
+           device="cpu", masked_m=None, masked_hi=None, **_):
+    """Masked batched MoE operands; masked_m ~ U{0..masked_hi} (masked_hi =
+    max_m unless given) unless masked_m is given."""
     cpu_gen = generator(seed, "cpu")
+    hi = max_m if masked_hi is None else masked_hi
     mm = masked_m if masked_m is not None else torch.randint(
-        0, max_m + 1, (num_groups,), generator=cpu_gen, dtype=torch.int64)
+        0, hi + 1, (num_groups,), generator=cpu_gen, dtype=torch.int64)
     mm = mm.to(torch.int32)
     gen = generator(seed + 7919, device)
     kb, nb = k // KBLOCK, n // NBLOCK
