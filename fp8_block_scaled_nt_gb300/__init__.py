@@ -84,6 +84,8 @@ def load():
         I64, I64, I64, I64, I64, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_size_t)]
     lib.fp8g_testing_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.fp8g_testing_set_wait_limit_ns.restype = None
+    lib.fp8g_testing_last_gemm_cta_pair.argtypes = []
+    lib.fp8g_testing_last_gemm_cta_pair.restype = ctypes.c_int
     for f in ("fp8_gemm_nt_groupwise", "fp8_group_gemm_contiguous", "fp8_batch_gemm_masked",
               "fused_add_rmsnorm_fp8_block_quant", "fused_moe_deepseek_fp8_block_scale", "bmm_fp8",
               "fused_moe_deepseek_fp8_block_scale_noalloc", "fp8g_get_device_status",

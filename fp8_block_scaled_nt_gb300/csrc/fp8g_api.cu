@@ -40,6 +40,10 @@ thread_local std::string t_last_error;
 // the timeout path shorten it through fp8g_testing_set_wait_limit_ns).
 thread_local uint64_t t_wait_limit_ns = fp8g::WAIT_LIMIT_NS;
 
+// Tile shape of this thread's last dense GEMM launch: 1 = CTA pairs, 0 = one
+// CTA per tile, -1 = none yet (fp8g_testing_last_gemm_cta_pair).
+thread_local int t_last_gemm_pair = -1;
+
 fp8g_status_t fail(fp8g_status_t s, const char* fmt, ...) {
     char buf[512];
     va_list ap;
@@ -127,11 +131,11 @@ struct MapKey {
     cuuint64_t dims[2];
     cuuint64_t stride;
     cuuint32_t box[2];
-    int dtype, l2;
+    int dtype, l2, swizzle;
     bool operator==(const MapKey& o) const {
         return base == o.base && dims[0] == o.dims[0] && dims[1] == o.dims[1] &&
                stride == o.stride && box[0] == o.box[0] && box[1] == o.box[1] &&
-               dtype == o.dtype && l2 == o.l2;
+               dtype == o.dtype && l2 == o.l2 && swizzle == o.swizzle;
     }
 };
 
@@ -146,8 +150,9 @@ MapCacheEntry g_map_cache[kMapCacheSlots];
 
 size_t map_key_hash(const MapKey& k) {
     uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
-    const uint64_t parts[7] = {k.dims[0], k.dims[1], k.stride, k.box[0], k.box[1],
-                               static_cast<uint64_t>(k.dtype), static_cast<uint64_t>(k.l2)};
+    const uint64_t parts[8] = {k.dims[0], k.dims[1], k.stride, k.box[0], k.box[1],
+                               static_cast<uint64_t>(k.dtype), static_cast<uint64_t>(k.l2),
+                               static_cast<uint64_t>(k.swizzle)};
     for (uint64_t v : parts) h = (h ^ v) * 0x100000001B3ull;
     return static_cast<size_t>(h ^ (h >> 29)) % kMapCacheSlots;
 }
@@ -156,9 +161,9 @@ size_t map_key_hash(const MapKey& k) {
 // `stride` = bytes between outer rows, `box` = {inner, outer} elements.
 fp8g_status_t encode_2d(CUtensorMap* map, const void* base, const cuuint64_t dims[2],
                         cuuint64_t stride, const cuuint32_t box[2], CUtensorMapDataType dtype,
-                        CUtensorMapL2promotion l2, const char* what) {
+                        CUtensorMapL2promotion l2, CUtensorMapSwizzle swizzle, const char* what) {
     MapKey key{base, {dims[0], dims[1]}, stride, {box[0], box[1]}, static_cast<int>(dtype),
-               static_cast<int>(l2)};
+               static_cast<int>(l2), static_cast<int>(swizzle)};
     const size_t slot = map_key_hash(key);
     {
         std::lock_guard<std::mutex> lock(g_map_mutex);
@@ -170,8 +175,8 @@ fp8g_status_t encode_2d(CUtensorMap* map, const void* base, const cuuint64_t dim
     cuuint64_t strides[1] = {stride};
     cuuint32_t elem_strides[2] = {1, 1};
     CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box,
-                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, l2,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(FP8G_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what,
                     static_cast<int>(r));
@@ -190,7 +195,8 @@ fp8g_status_t encode_map(CUtensorMap* map, const void* base, int64_t rows, int64
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(fp8g::BLOCK_K),
                                static_cast<cuuint32_t>(box_rows)};
     return encode_2d(map, base, dims, static_cast<cuuint64_t>(k), box,
-                     CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, what);
+                     CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_SWIZZLE_128B, what);
 }
 
 // Row-major output of `rows` x `n` elements of `esz` bytes as a 2-D TMA view for
@@ -203,7 +209,7 @@ fp8g_status_t encode_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t
                                static_cast<cuuint32_t>(box_rows)};
     return encode_2d(map, base, dims, static_cast<cuuint64_t>(n * esz), box,
                      esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                     CU_TENSOR_MAP_L2_PROMOTION_NONE, "out");
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_SWIZZLE_128B, "out");
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -569,6 +575,7 @@ fp8g_status_t fp8_gemm_nt_groupwise(const void* a, const void* b, const float* a
             FP8G_OK)
             return s;
         Params p = base_params(a_scale, b_scale, out, m, n, k, tile_m);
+        t_last_gemm_pair = pair ? 1 : 0;
         p.num_tiles = static_cast<int>(tiles);
         p.num_groups = 1;
         p.scale_mn_major = scale_major == FP8G_SCALE_MN_MAJOR;
@@ -951,6 +958,8 @@ fp8g_status_t fp8g_get_stream_status(unsigned int* flags, int clear, cudaStream_
 void fp8g_testing_set_wait_limit_ns(uint64_t ns) {
     t_wait_limit_ns = ns ? ns : fp8g::WAIT_LIMIT_NS;
 }
+
+int fp8g_testing_last_gemm_cta_pair(void) { return t_last_gemm_pair; }
 
 fp8g_status_t fp8g_get_device_status(unsigned int* flags, int clear) {
     try {
