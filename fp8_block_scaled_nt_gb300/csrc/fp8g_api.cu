@@ -60,8 +60,8 @@ fp8g_status_t cuda_fail(cudaError_t e, const char* what) {
 
 constexpr int kMaxDevices = 64;
 // dense bf16, dense f16 (single CTA), grouped, masked, dense bf16, dense f16 (CTA pair),
-// dense E4M3 (single CTA), dense E4M3 (CTA pair), bmm bf16, bmm f16
-constexpr int kNumKernels = 10;
+// dense E4M3 (single CTA), dense E4M3 (CTA pair), bmm bf16, bmm f16, masked (CTA pair)
+constexpr int kNumKernels = 11;
 
 struct DeviceState {
     bool probed = false;
@@ -664,17 +664,30 @@ fp8g_status_t fp8_batch_gemm_masked(const void* a, const void* b, const float* a
             return fail(FP8G_ERR_INVALID_ARGUMENT, "masked_m must be 4-byte aligned");
         DeviceState* ds = nullptr;
         if ((s = device_state(&ds)) != FP8G_OK) return s;
+        // expected_m (the page's kernel-selection hint) picks the tile shape:
+        // when a typical group holds more than 128 rows, CTA pairs compute 256-row
+        // tiles (a third less operand traffic per SM); otherwise one CTA per
+        // 128-row tile, which wastes less on short groups.  Results are the same
+        // bits either way.
+        const bool pair = expected_m > fp8g::BLOCK_M && max_m > fp8g::BLOCK_M;
+        const int tile_m = pair ? 2 * fp8g::BLOCK_M : fp8g::BLOCK_M;
+        const int64_t max_tiles = num_groups * ((max_m + tile_m - 1) / tile_m) * ((n + 255) / 256);
         CUtensorMap map_a, map_b;
         if ((s = encode_map(&map_a, a, num_groups * max_m, k, fp8g::BLOCK_M, "a")) != FP8G_OK)
             return s;
-        if ((s = encode_map(&map_b, b, num_groups * n, k, fp8g::BLOCK_N, "b")) != FP8G_OK)
+        if ((s = encode_map(&map_b, b, num_groups * n, k,
+                            pair ? fp8g::BLOCK_N / 2 : fp8g::BLOCK_N, "b")) != FP8G_OK)
             return s;
-        Params p = base_params(a_scale, b_scale, out, max_m, n, k);
-        p.num_tiles = static_cast<int>(tiles);  // upper bound; the kernel walks masked_m
+        Params p = base_params(a_scale, b_scale, out, max_m, n, k, tile_m);
+        p.num_tiles = static_cast<int>(max_tiles);  // upper bound; the kernel walks masked_m
         p.num_groups = static_cast<int>(num_groups);
         p.masked_m = masked_m;
         p.status = ds->status;
-        return launch<fp8g::FORM_MASKED, __nv_bfloat16, false>(*ds, 3, map_a, map_b, p, tiles, stream);
+        if (pair)
+            return launch<fp8g::FORM_MASKED, __nv_bfloat16, true>(*ds, 10, map_a, map_b, p,
+                                                                  max_tiles, stream);
+        return launch<fp8g::FORM_MASKED, __nv_bfloat16, false>(*ds, 3, map_a, map_b, p, max_tiles,
+                                                                stream);
     } catch (...) {
         return fail(FP8G_ERR_CUDA, "unexpected exception");
     }

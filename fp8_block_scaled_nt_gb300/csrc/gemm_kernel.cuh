@@ -170,7 +170,7 @@ __device__ __forceinline__ int tile_stride() {
 template <int FORM, bool PAIR>
 struct Scheduler {
     using C = Cfg<PAIR, FORM>;
-    static_assert(!PAIR || FORM == FORM_DENSE, "CTA pairs serve the dense form");
+    static_assert(!PAIR || FORM != FORM_GROUPED, "CTA pairs serve the dense and masked forms");
     const Params& p;
     const int rank;
     int g = 0;     // masked: group the cursor is in
@@ -205,7 +205,7 @@ struct Scheduler {
         if constexpr (FORM == FORM_MASKED) {
             while (g < p.num_groups) {
                 const int rows_g = masked_rows(g, flag && blockIdx.x == 0);
-                const int mbk = (rows_g + BLOCK_M - 1) / BLOCK_M;
+                const int mbk = (rows_g + C::TILE_M - 1) / C::TILE_M;
                 const int count = mbk * p.n_tiles;
                 if (t < base + count) {
                     const int local = t - base;
@@ -213,8 +213,8 @@ struct Scheduler {
                     tile.mb = local - tile.nb * mbk;
                     tile.group = g;
                     tile.group_rows = rows_g;
-                    tile.row0 = g * p.rows + tile.mb * BLOCK_M;
-                    tile.b_row0 = g * p.n + tile.nb * BLOCK_N;
+                    tile.row0 = g * p.rows + tile.mb * C::TILE_M + rank * BLOCK_M;
+                    tile.b_row0 = g * p.n + tile.nb * BLOCK_N + rank * C::B_ROWS;
                     return true;
                 }
                 base += count;
@@ -705,7 +705,7 @@ __device__ __forceinline__ RowScales row_scales(const Params& p, const Tile& til
     x.sa = x.sb = nullptr;
     x.sa_step = x.sb_step = 1;
     if constexpr (FORM == FORM_MASKED) {
-        const int rin = tile.mb * BLOCK_M + r;
+        const int rin = tile.row0 - tile.group * p.rows + r;  // row within the group
         x.out_row = static_cast<int64_t>(tile.group) * p.rows + rin;
         x.row_ok = rin < tile.group_rows;
         if (rin < p.rows) x.sa = p.a_scale + x.out_row * KB;

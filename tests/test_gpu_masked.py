@@ -18,18 +18,22 @@ def _run(fp8g, w, expected_m=None):
     return out
 
 
+# expected_m picks the tile shape: a hint above 128 (with max_m above 128) runs
+# 256-row tiles on CTA pairs, otherwise one CTA per 128-row tile
+@pytest.mark.parametrize("hint", ["low", "high"])
 @pytest.mark.parametrize("masked,max_m,n,k", [((0, 1, 130, 256), 256, 384, 256),
                                               ((5, 77), 100, 128, 384),
-                                              ((129, 128, 3), 200, 256, 512)])
-def test_small_full_parity(fp8g, oracle_mod, masked, max_m, n, k):
+                                              ((129, 128, 3), 200, 256, 512),
+                                              ((255, 40, 0, 256, 300), 300, 512, 640)])
+def test_small_full_parity(fp8g, oracle_mod, masked, max_m, n, k, hint):
     mm = torch.tensor(masked, dtype=torch.int32)
     w = workloads.masked(len(masked), max_m, n, k, seed=max_m + n + k, masked_m=mm)
-    out = _run(fp8g, w)
+    out = _run(fp8g, w, expected_m=1 if hint == "low" else max_m)
     ref, _, written = oracle_mod.batch_gemm_masked(w["a"], w["b"], w["a_scale"], w["b_scale"],
                                                    w["masked_m"])
     rows = written.any(axis=2)
     assert np.array_equal(written_rows(out), rows)
-    assert_close(as_f64(out)[rows], ref[rows], "masked %s" % (masked,))
+    assert_close(as_f64(out)[rows], ref[rows], "masked %s %s" % (masked, hint))
     assert fp8g.get_device_status() == 0
 
 
