@@ -386,9 +386,11 @@ fp8g_status_t grouped_gemm(DeviceState& ds, const void* a, const void* b, const 
     if ((s = encode_map(&map_a, a, m, k, fp8g::BLOCK_M, "a")) != FP8G_OK) return s;
     if ((s = encode_map(&map_b, b, num_groups * n, k, fp8g::BLOCK_N, "b")) != FP8G_OK) return s;
     Params p = base_params(a_scale, b_scale, out, m, n, k);
-    // bands of 4 m-blocks: fewer bands straddle two experts' segments, whose
-    // weights then stream twice (measured best of 4-32 on 4096 tokens x top-8
-    // over 64 experts)
+    // tiles ordered by expert segment where the segment table fits; else bands
+    // of 4 m-blocks (fewer bands straddle two experts' segments, whose weights
+    // then stream twice; measured best of 4-32 on 4096 tokens x top-8 over 64
+    // experts)
+    p.seg_raster = p.m_blocks <= fp8g::SEG_RASTER_MAX_BLOCKS;
     p.band_m = 4;
     p.num_tiles = static_cast<int>(tiles);
     p.num_groups = static_cast<int>(num_groups);

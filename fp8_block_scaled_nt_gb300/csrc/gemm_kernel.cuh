@@ -91,6 +91,11 @@ constexpr uint64_t ABORT_GRACE_NS = 5000000ull;  // 5 ms
 
 enum Form { FORM_DENSE = 0, FORM_GROUPED = 1, FORM_MASKED = 2 };
 
+// Grouped form: up to this many 128-row blocks, tiles are ordered expert
+// segment by expert segment (a table of segment starts in shared memory);
+// beyond it, by bands of band_m blocks.
+constexpr int SEG_RASTER_MAX_BLOCKS = 4096;
+
 // Geometry of the pipeline variants.  Ring depths: shared memory left over
 // becomes L1, which the per-row scale loads of the promotion warps live on, so
 // the rings are as deep as the copies need and no deeper (measured); the
@@ -109,9 +114,13 @@ struct Cfg {
     static constexpr int A_BYTES = BLOCK_M * BLOCK_K;
     static constexpr int B_BYTES = B_ROWS * BLOCK_K;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    // grouped form: the expert-segment table (count, starts, end sentinel)
+    static constexpr int SEG_BYTES =
+        FORM == FORM_GROUPED ? ((SEG_RASTER_MAX_BLOCKS + 2) * 4 + 15) / 16 * 16 : 0;
+    static constexpr size_t SEG_OFFSET = size_t(STAGES) * STAGE_BYTES + 2 * OUT_BYTES;
     static constexpr size_t SMEM_BYTES = 1024 /* alignment slack */ +
                                          size_t(STAGES) * STAGE_BYTES + 2 * OUT_BYTES +
-                                         BAR_BYTES;
+                                         SEG_BYTES + BAR_BYTES;
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
     static constexpr uint32_t IDESC = idesc_e4m3_f32(TILE_M, BLOCK_N);
 };
@@ -133,6 +142,7 @@ struct Params {
     int scale_mn_major;  // dense form only
     const float* out_scale;  // dense form with E4M3 output: the output's FP32 scale
     int band_m;          // m-blocks per raster band (dense/grouped)
+    int seg_raster;      // grouped: order tiles by expert segment (see Scheduler)
     // bmm_fp8 (bmm_kernel.cuh): rows = m of one batch, k of one batch
     int batch;
     int a_channelwise, b_channelwise;  // scales per row of A / column of B, else one value
@@ -150,6 +160,38 @@ struct Tile {
     int row_expert[4];   // grouped: m_indices of rows 32q + lane, q = 0..3
     bool skip;           // grouped: padding-only block or broken precondition
 };
+
+// The kernel's shared memory, 1024-byte aligned (the base every role agrees on).
+__device__ __forceinline__ uint8_t* smem_base() {
+    extern __shared__ uint8_t smem_raw[];
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
+}
+
+// Grouped form: the starts of the runs of 128-row blocks whose first rows carry
+// the same m_indices value -- the experts' segments of the contiguous layout
+// (and runs of padding-only blocks) -- written by one warp into
+// table[1 .. count], with table[0] = count and table[count + 1] = m_blocks.
+__device__ __forceinline__ void build_segments(const Params& p, int* table) {
+    const int lane = threadIdx.x & 31;
+    int count = 0, prev = INT_MIN;
+    for (int b0 = 0; b0 < p.m_blocks; b0 += 32) {
+        const int b = b0 + lane;
+        const int key = b < p.m_blocks ? __ldg(p.m_indices + static_cast<int64_t>(b) * BLOCK_M)
+                                       : INT_MIN;
+        int left = __shfl_up_sync(0xffffffffu, key, 1);
+        if (lane == 0) left = prev;
+        const bool start = b < p.m_blocks && (b == 0 || key != left);
+        const uint32_t mask = __ballot_sync(0xffffffffu, start);
+        if (start) table[1 + count + __popc(mask & ((1u << lane) - 1u))] = b;
+        count += __popc(mask);
+        prev = __shfl_sync(0xffffffffu, key, 31);
+    }
+    if (lane == 0) {
+        table[0] = count;
+        table[1 + count] = p.m_blocks;
+    }
+}
 
 // Tile ids this CTA (or CTA pair) walks: first, first + stride, ...
 template <bool PAIR>
@@ -196,6 +238,27 @@ struct Scheduler {
         mb = band * p.band_m + rem % in_band;
     }
 
+    // Grouped form: tiles expert segment by expert segment, and within a
+    // segment n-block by n-block with the segment's 128-row blocks fastest, so
+    // the CTAs running at one time share one expert's weights (which then
+    // stream from memory once) and its rows.  The tiles before segment s are
+    // n_tiles x its first block.
+    __device__ void segment_raster(int t, int& mb, int& nb) const {
+        const int* table = reinterpret_cast<const int*>(smem_base() + C::SEG_OFFSET);
+        int lo = 0, hi = table[0] - 1;  // the last segment starting at or before t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (table[1 + mid] * p.n_tiles <= t)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int start = table[1 + lo], len = table[2 + lo] - start;
+        const int local = t - start * p.n_tiles;
+        nb = local / len;
+        mb = start + (local - nb * len);
+    }
+
     // False once t is past the last tile.  `flag` lets one thread report
     // precondition violations in the device status word.
     __device__ bool next(int t, Tile& tile, bool flag) {
@@ -223,7 +286,10 @@ struct Scheduler {
             return false;
         } else {
             if (t >= p.num_tiles) return false;
-            raster(t, tile.mb, tile.nb);
+            if (FORM == FORM_GROUPED && p.seg_raster)
+                segment_raster(t, tile.mb, tile.nb);
+            else
+                raster(t, tile.mb, tile.nb);
             tile.row0 = tile.mb * C::TILE_M + rank * BLOCK_M;
             tile.b_row0 = tile.nb * BLOCK_N + rank * C::B_ROWS;
             if constexpr (FORM == FORM_GROUPED) {
@@ -900,7 +966,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::STAGES * C::A_BYTES;
     uint8_t* sOut = sB + C::STAGES * C::B_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 2 * C::OUT_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::SEG_OFFSET + C::SEG_BYTES);
     uint64_t* empty = full + C::STAGES;
     uint64_t* acc_full = empty + C::STAGES;
     uint64_t* acc_empty = acc_full + 2;
@@ -958,6 +1024,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // stream serialization); global memory is read and written only after it.
     grid_dependency_wait();
     grid_launch_dependents();
+    if constexpr (FORM == FORM_GROUPED) {
+        if (p.seg_raster) {  // every role's scheduler reads the table
+            if (warp == 0) build_segments(p, reinterpret_cast<int*>(smem + C::SEG_OFFSET));
+            __syncthreads();
+        }
+    }
 
     if (warp < FIRST_PROMO_WARP) {
         regs_dec<CONTROL_REGS>();
