@@ -9,8 +9,10 @@
 //
 // Persistent, one CTA per SM, 384 threads, 128 x 256 output tiles:
 //   warp 0      TMA producer: per 128-K block an A tile (128 rows x 128 k,
-//               K-major) and B as two 128-column halves of 128 k-rows (the
-//               operand stays N-major, as B is stored), into a 4-slot ring.
+//               K-major) and B as two 128-column halves of 128 k-rows of the
+//               tile's batch (the operand stays N-major, as B is stored), into
+//               a 4-slot ring.  n and k need only be multiples of 16: the last
+//               K block's k past k, and columns past n, read as zero.
 //   warp 1      MMA issuer (one thread): per tile KB x 4 tcgen05.mma (K = 32)
 //               accumulating into TMEM buffer (tile index mod 2) of 256
 //               columns, B read as an MN-major operand; one commit per tile.
@@ -21,7 +23,8 @@
 //               issuer has nothing else to wait for, so one keeps the pipe fed.
 //   warps 4-11  epilogue: read the tile's FP32 sums from TMEM once, multiply by
 //               a_scale(row) * b_scale(column), round to BF16/FP16 through the
-//               shared-memory staging slice (store_tile_rows), release the buffer.
+//               shared-memory staging slice (store_tile_rows: rows past m and
+//               columns past n are not written), release the buffer.
 //   warps 2-3   idle (they complete warpgroup 0 for the register split).
 // The two buffers let the next tile's MMAs run while a tile's epilogue runs.
 // Every pipeline wait is bounded as in gemm_kernel.cuh.
@@ -60,7 +63,6 @@ struct BmmTile {
     int bb;     // batch
     int rin0;   // first row of the tile within the batch
     int row0;   // first row in the (batch * m) x k view of A (and of out)
-    int krow0;  // first row of the batch in the (batch * k) x n view of B
     int n0;     // first column
 };
 
@@ -79,7 +81,6 @@ __device__ __forceinline__ bool bmm_tile(const Params& p, int t, BmmTile& tile) 
     tile.bb = bb;
     tile.rin0 = mb * BLOCK_M;
     tile.row0 = bb * p.rows + mb * BLOCK_M;
-    tile.krow0 = bb * p.k;
     tile.n0 = nb * BLOCK_N;
     return true;
 }
@@ -104,9 +105,9 @@ __device__ __forceinline__ void bmm_producer(const CUtensorMap* map_a, const CUt
                 tma_load_2d(sA + stage * BMM_A_BYTES, map_a, full + stage, kb * BLOCK_K,
                             tile.row0);
                 uint8_t* b = sB + stage * BMM_B_BYTES;
-                tma_load_2d(b, map_b, full + stage, tile.n0, tile.krow0 + kb * BLOCK_K);
-                tma_load_2d(b + BMM_B_HALF_BYTES, map_b, full + stage, tile.n0 + 128,
-                            tile.krow0 + kb * BLOCK_K);
+                tma_load_3d(b, map_b, full + stage, tile.n0, kb * BLOCK_K, tile.bb);
+                tma_load_3d(b + BMM_B_HALF_BYTES, map_b, full + stage, tile.n0 + 128,
+                            kb * BLOCK_K, tile.bb);
                 armed |= 1u << stage;
                 armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == BMM_STAGES) {
@@ -197,6 +198,7 @@ __device__ __forceinline__ void bmm_epilogue(const Params& p, uint64_t* acc_full
         const bool row_ok = rin < p.rows;
         const int col0 = tile.n0 + half * 128;
         const bool col_ok = col0 < p.n;  // uniform over the warpgroup
+        const int cols = min(128, p.n - col0);  // columns of this half inside n
         const int64_t out_row = static_cast<int64_t>(tile.bb) * p.rows + rin;
         const float sa = p.a_channelwise
                              ? (row_ok ? __ldg(p.a_scale + static_cast<int64_t>(tile.bb) * p.rows +
@@ -218,12 +220,15 @@ __device__ __forceinline__ void bmm_epilogue(const Params& p, uint64_t* acc_full
                     uint32_t v[16];
                     tmem_load_16cols_async(taddr + c * 16, v);
                     tmem_wait_16(v);
+                    // n is a multiple of 16: a 16-column chunk is all inside n or
+                    // all past it (its channelwise scales do not exist)
+                    const bool chunk_in = c * 16 < cols;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         float s0 = sb1, s1 = sb1;
                         if (p.b_channelwise) {
-                            s0 = __ldg(sb + c * 16 + 2 * i);
-                            s1 = __ldg(sb + c * 16 + 2 * i + 1);
+                            s0 = chunk_in ? __ldg(sb + c * 16 + 2 * i) : 0.0f;
+                            s1 = chunk_in ? __ldg(sb + c * 16 + 2 * i + 1) : 0.0f;
                         }
                         acc[c * 8 + i] = pack_f32x2(__uint_as_float(v[2 * i]) * (sa * s0),
                                                     __uint_as_float(v[2 * i + 1]) * (sa * s1));
@@ -236,7 +241,7 @@ __device__ __forceinline__ void bmm_epilogue(const Params& p, uint64_t* acc_full
         }
         if (col_ok)
             store_tile_rows<OutT>(out, p.n, out_row - r, col0, ok && row_ok, acc,
-                                  sOut + half * OUT_STAGE_BYTES, 1 + half, 1.0f);
+                                  sOut + half * OUT_STAGE_BYTES, 1 + half, 1.0f, cols);
         if (named_barrier_or(1 + half, 128, !ok)) break;
     }
 }

@@ -128,14 +128,18 @@ fp8g_status_t device_state(DeviceState** out) {
 // hash of the key; a collision replaces the entry.
 struct MapKey {
     const void* base;
-    cuuint64_t dims[2];
-    cuuint64_t stride;
-    cuuint32_t box[2];
+    int rank;
+    cuuint64_t dims[3];
+    cuuint64_t strides[2];
+    cuuint32_t box[3];
     int dtype, l2, swizzle;
     bool operator==(const MapKey& o) const {
-        return base == o.base && dims[0] == o.dims[0] && dims[1] == o.dims[1] &&
-               stride == o.stride && box[0] == o.box[0] && box[1] == o.box[1] &&
-               dtype == o.dtype && l2 == o.l2 && swizzle == o.swizzle;
+        if (base != o.base || rank != o.rank || dtype != o.dtype || l2 != o.l2 ||
+            swizzle != o.swizzle)
+            return false;
+        for (int i = 0; i < 3; ++i)
+            if (dims[i] != o.dims[i] || box[i] != o.box[i]) return false;
+        return strides[0] == o.strides[0] && strides[1] == o.strides[1];
     }
 };
 
@@ -150,20 +154,33 @@ MapCacheEntry g_map_cache[kMapCacheSlots];
 
 size_t map_key_hash(const MapKey& k) {
     uint64_t h = reinterpret_cast<uintptr_t>(k.base) * 0x9E3779B97F4A7C15ull;
-    const uint64_t parts[8] = {k.dims[0], k.dims[1], k.stride, k.box[0], k.box[1],
-                               static_cast<uint64_t>(k.dtype), static_cast<uint64_t>(k.l2),
-                               static_cast<uint64_t>(k.swizzle)};
+    const uint64_t parts[12] = {static_cast<uint64_t>(k.rank), k.dims[0], k.dims[1], k.dims[2],
+                                k.strides[0], k.strides[1], k.box[0], k.box[1], k.box[2],
+                                static_cast<uint64_t>(k.dtype), static_cast<uint64_t>(k.l2),
+                                static_cast<uint64_t>(k.swizzle)};
     for (uint64_t v : parts) h = (h ^ v) * 0x100000001B3ull;
     return static_cast<size_t>(h ^ (h >> 29)) % kMapCacheSlots;
 }
 
-// 2-D tiled map with 128-byte swizzle: `dims` = {inner, outer} elements,
-// `stride` = bytes between outer rows, `box` = {inner, outer} elements.
-fp8g_status_t encode_2d(CUtensorMap* map, const void* base, const cuuint64_t dims[2],
-                        cuuint64_t stride, const cuuint32_t box[2], CUtensorMapDataType dtype,
-                        CUtensorMapL2promotion l2, CUtensorMapSwizzle swizzle, const char* what) {
-    MapKey key{base, {dims[0], dims[1]}, stride, {box[0], box[1]}, static_cast<int>(dtype),
-               static_cast<int>(l2), static_cast<int>(swizzle)};
+// Tiled map of rank 2 or 3: `dims` = extents in elements, innermost first;
+// `strides` = bytes between consecutive indices of dimensions 1 .. rank-1;
+// `box` = the copied tile's extents.  Elements outside the extents read as
+// zero.
+fp8g_status_t encode_tiled(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                           const cuuint64_t* strides, const cuuint32_t* box,
+                           CUtensorMapDataType dtype, CUtensorMapL2promotion l2,
+                           CUtensorMapSwizzle swizzle, const char* what) {
+    MapKey key{};
+    key.base = base;
+    key.rank = rank;
+    for (int i = 0; i < rank; ++i) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+        if (i + 1 < rank) key.strides[i] = strides[i];
+    }
+    key.dtype = static_cast<int>(dtype);
+    key.l2 = static_cast<int>(l2);
+    key.swizzle = static_cast<int>(swizzle);
     const size_t slot = map_key_hash(key);
     {
         std::lock_guard<std::mutex> lock(g_map_mutex);
@@ -172,10 +189,10 @@ fp8g_status_t encode_2d(CUtensorMap* map, const void* base, const cuuint64_t dim
             return FP8G_OK;
         }
     }
-    cuuint64_t strides[1] = {stride};
-    cuuint32_t elem_strides[2] = {1, 1};
-    CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box,
-                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, l2,
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = g_encode(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
+                          key.dims, key.strides, key.box, elem_strides,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, l2,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(FP8G_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what,
@@ -185,6 +202,14 @@ fp8g_status_t encode_2d(CUtensorMap* map, const void* base, const cuuint64_t dim
     g_map_cache[slot].key = key;
     g_map_cache[slot].map = *map;
     return FP8G_OK;
+}
+
+// 2-D tiled map: `dims` = {inner, outer} elements, `stride` = bytes between
+// outer rows, `box` = {inner, outer} elements.
+fp8g_status_t encode_2d(CUtensorMap* map, const void* base, const cuuint64_t dims[2],
+                        cuuint64_t stride, const cuuint32_t box[2], CUtensorMapDataType dtype,
+                        CUtensorMapL2promotion l2, CUtensorMapSwizzle swizzle, const char* what) {
+    return encode_tiled(map, base, 2, dims, &stride, box, dtype, l2, swizzle, what);
 }
 
 // Row-major E4M3 matrix of `rows` x `k` bytes as a 2-D TMA view, tile
@@ -803,10 +828,17 @@ fp8g_status_t bmm_fp8(const void* a, const void* b, fp8g_fp8_format_t a_format,
         if (out_dtype != FP8G_OUT_BF16 && out_dtype != FP8G_OUT_F16)
             return fail(FP8G_ERR_INVALID_ARGUMENT, "out_dtype %d is neither BF16 nor FP16",
                         (int)out_dtype);
-        fp8g_status_t s = check_nk(n, k);
-        if (s != FP8G_OK) return s;
-        if (batch * m > kMaxDim || batch * k > kMaxDim || batch * n > kMaxDim)
-            return fail(FP8G_ERR_UNSUPPORTED, "batch * m, batch * k, batch * n must be < 2^31");
+        // n and k need only be multiples of 16: TMA views want 16-byte row
+        // pitches; the tails of the last 128-wide blocks read as zero.
+        if (n <= 0 || n % 16)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "n = %lld must be a positive multiple of 16",
+                        (long long)n);
+        if (k <= 0 || k % 16)
+            return fail(FP8G_ERR_INVALID_ARGUMENT, "k = %lld must be a positive multiple of 16",
+                        (long long)k);
+        fp8g_status_t s = FP8G_OK;
+        if (n > kMaxDim || k > kMaxDim || batch * m > kMaxDim || batch * n > kMaxDim)
+            return fail(FP8G_ERR_UNSUPPORTED, "n, k, batch * m and batch * n must be < 2^31");
         const int64_t m_blocks = (m + 127) / 128, n_tiles = (n + 255) / 256;
         const int64_t tiles = batch * m_blocks * n_tiles;
         if (tiles > kMaxDim) return fail(FP8G_ERR_UNSUPPORTED, "problem has too many tiles");
@@ -818,10 +850,26 @@ fp8g_status_t bmm_fp8(const void* a, const void* b, fp8g_fp8_format_t a_format,
         DeviceState* ds = nullptr;
         if ((s = device_state(&ds)) != FP8G_OK) return s;
         CUtensorMap map_a, map_b;
+        // A: (batch * m) rows of k; a K block past k reads zeros.  A tile's rows
+        // past m belong to the next batch (or read as zero); they are not stored.
         if ((s = encode_map(&map_a, a, batch * m, k, fp8g::BLOCK_M, "a")) != FP8G_OK) return s;
-        // B stays N-major: rows are k (of every batch), 128-column boxes
-        if ((s = encode_map(&map_b, b, batch * k, n, 128, "b")) != FP8G_OK) return s;
+        // B stays N-major, as a 3-D view (n, k, batch) in boxes of 128 columns x
+        // 128 k-rows of one batch: k-rows past k read as zero rather than as the
+        // next batch's rows, so no value of another batch (an infinity or NaN
+        // of E5M2) meets the zeros of A's tail.
+        {
+            const cuuint64_t dims[3] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(k),
+                                        static_cast<cuuint64_t>(batch)};
+            const cuuint64_t strides[2] = {static_cast<cuuint64_t>(n),
+                                           static_cast<cuuint64_t>(n) * static_cast<cuuint64_t>(k)};
+            const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(fp8g::BLOCK_K), 1};
+            if ((s = encode_tiled(&map_b, b, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  "b")) != FP8G_OK)
+                return s;
+        }
         Params p = base_params(a_scale, b_scale, out, m, n, k);
+        p.kblocks = static_cast<int>((k + fp8g::BLOCK_K - 1) / fp8g::BLOCK_K);
         p.band_m = 8;
         p.num_tiles = static_cast<int>(tiles);
         p.batch = static_cast<int>(batch);

@@ -134,7 +134,7 @@ struct Params {
     unsigned int* status;      // device status word
     int rows;                  // dense: m; grouped: M_total; masked: max_m
     int n, k;
-    int kblocks, nblocks;  // k/128, n/128
+    int kblocks, nblocks;  // k/128, n/128 (bmm_fp8: kblocks = ceil(k/128))
     int n_tiles;           // ceil(n / BLOCK_N)
     int m_blocks;          // ceil(rows / TILE_M)
     int num_tiles;         // dense/grouped: m_blocks * n_tiles
@@ -553,12 +553,13 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
 // memory (16-byte chunk c of row r at chunk c ^ (r % 8), so that the 32 rows
 // a warp writes at once spread over all banks); then each warp stores the 32
 // rows it owns as full 128-byte segments, four rows per instruction, skipping
-// rows outside the form.  `row_base` is the output row of tile row 0.
+// rows outside the form.  `row_base` is the output row of tile row 0; `cols`
+// (a multiple of 16 / sizeof(OutT)) the columns from col0 that exist.
 template <typename OutT>
 __device__ __forceinline__ void store_tile_rows(OutT* out, int64_t n, int64_t row_base, int col0,
                                                 bool row_ok, const uint64_t (&acc)[64],
                                                 uint8_t* staging, uint32_t barrier_id,
-                                                float out_inv) {
+                                                float out_inv, int cols = 128) {
     constexpr int ESZ = static_cast<int>(sizeof(OutT));  // 2 (BF16/FP16) or 1 (E4M3)
     constexpr int PASSES = ESZ;                          // 128 columns x ESZ bytes
     constexpr int PASS_COLS = 128 / ESZ;
@@ -601,9 +602,9 @@ __device__ __forceinline__ void store_tile_rows(OutT* out, int64_t n, int64_t ro
             const int rr = quarter * 32 + i;    // row within the tile
             const bool ok_i = __shfl_sync(0xffffffffu, row_ok ? 1 : 0, i) != 0;
             const uint4 v = ld_shared_v4(base + rr * 128 + ((chunk ^ (rr & 7)) << 4));
-            if (ok_i)
-                *reinterpret_cast<uint4*>(out + (row_base + rr) * n + col0 + pass * PASS_COLS +
-                                          chunk * (16 / ESZ)) = v;
+            const int col = pass * PASS_COLS + chunk * (16 / ESZ);
+            if (ok_i && col < cols)
+                *reinterpret_cast<uint4*>(out + (row_base + rr) * n + col0 + col) = v;
         }
         named_barrier_sync(barrier_id, 128);  // staging free for the next pass
     }

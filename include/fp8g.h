@@ -117,8 +117,10 @@ fp8g_status_t fp8_gemm_nt_groupwise(const void* a, const void* b,
  *
  * The sum over k is accumulated in FP32 on the tensor cores (no per-block
  * promotion is needed, as the scales do not depend on k) and scaled once.
- * n and k must be positive multiples of 128; batch and m may be 0.  a, b, out
- * 16-byte aligned, scales 4-byte aligned.
+ * n and k must be positive multiples of 16 (TMA reads rows whose pitch is a
+ * multiple of 16 bytes; the page states no constraint); batch and m may be 0.
+ * a, b, out 16-byte aligned, scales 4-byte aligned.  Otherwise
+ * FP8G_ERR_INVALID_ARGUMENT, nothing launched.
  */
 fp8g_status_t bmm_fp8(const void* a, const void* b, fp8g_fp8_format_t a_format,
                       fp8g_fp8_format_t b_format, const float* a_scale, int a_channelwise,

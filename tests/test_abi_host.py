@@ -184,6 +184,41 @@ def test_moe_noalloc_rejects_oversize_on_the_host(lib):
     assert rc == 2 and "static scratch" in lib.last_error()
 
 
+def _bmm(h, a=16, b=16, af=0, bf=0, sa=16, ach=0, sb=16, bch=0, out=16, dt=0, batch=2, m=100,
+         n=208, k=176):
+    return h.bmm_fp8(a, b, af, bf, sa, ach, sb, bch, out, dt, batch, m, n, k, None)
+
+
+@pytest.mark.parametrize("kwargs,status,msg", [
+    (dict(k=100), 1, "k = 100"),
+    (dict(k=0), 1, "k = 0"),
+    (dict(n=200), 1, "n = 200"),
+    (dict(n=-16), 1, "n = -16"),
+    (dict(m=-1), 1, "m = -1"),
+    (dict(af=2), 1, "E4M3 or E5M2"),
+    (dict(dt=2), 1, "out_dtype"),
+    (dict(b=0), 1, "null"),
+    (dict(out=24), 1, "16-byte"),
+    (dict(sb=18), 1, "4-byte"),
+    (dict(n=1 << 31), 2, "2^31"),
+])
+def test_bmm_host_validation(lib, kwargs, status, msg):
+    h = lib.load()
+    assert _bmm(h, **kwargs) == status
+    assert msg in lib.last_error()
+
+
+def test_bmm_accepts_multiples_of_16_and_empty_problems(lib):
+    import torch
+    h = lib.load()
+    assert _bmm(h, m=0, a=0, out=0, sa=0) == 0
+    assert _bmm(h, batch=0, a=0, b=0, out=0) == 0
+    if not torch.cuda.is_available():
+        # n = 208, k = 176 pass the shape checks; the call then needs a device
+        assert _bmm(h) == 4 and "cudaGetDevice" in lib.last_error()
+        assert _bmm(h, n=16, k=16) == 4
+
+
 def test_valid_call_without_a_device_reports_cuda_error(lib):
     import torch
     if torch.cuda.is_available():

@@ -107,8 +107,54 @@ def test_bmm_workload_sampled(fp8g, oracle_mod):
         assert_close(got.reshape(-1), ref.reshape(-1), "bmm workload batch %d" % bb)
 
 
+@pytest.mark.parametrize("a_fmt,b_fmt", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("channelwise", [False, True])
+@pytest.mark.parametrize("shape", [(2, 200, 208, 176), (1, 130, 80, 48), (3, 65, 400, 272),
+                                   (1, 1, 16, 16), (2, 257, 528, 1040)])
+def test_ragged_n_and_k_parity_and_no_write_past_the_output(fp8g, oracle_mod, a_fmt, b_fmt,
+                                                            channelwise, shape):
+    # n and k multiples of 16 but not of 128: the last K block's tail and the
+    # columns past n read as zero; nothing past (batch, m, n) is written (the
+    # output sits at the start of a larger sentinel buffer)
+    batch, m, n, k = shape
+    a, b, sa, sb = operands(batch, m, n, k, a_fmt, b_fmt, channelwise,
+                            seed=sum(shape) + 7 * a_fmt + b_fmt)
+    size = batch * m * n
+    buf = sentinel_like((size + 4096,), torch.bfloat16, "cuda")
+    guard = buf[size:].clone()
+    out = buf[:size].view(batch, m, n)
+    fp8g.bmm_fp8(a.cuda(), b.cuda(), sa.cuda(), sb.cuda(), out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(buf[size:].view(torch.int16), guard.view(torch.int16))
+    ref, _ = oracle_mod.bmm_fp8(a.view(torch.uint8), b.view(torch.uint8), sa.numpy(), sb.numpy(),
+                                a_fmt, b_fmt)
+    assert_close(out.float().cpu().double().numpy().reshape(-1), ref.reshape(-1),
+                 "bmm ragged %s %s %s" % (shape, a_fmt, b_fmt))
+
+
+def test_k_tail_reads_no_row_of_the_next_batch(fp8g, oracle_mod):
+    # k = 176: the last K block covers k-rows 128..255 of each batch.  The rows
+    # past k must read as zero, not as the next batch's first rows: plant
+    # infinities (E5M2) there, so a read of them would turn batch 0 into NaN.
+    batch, m, n, k = 2, 130, 272, 176
+    a, b, sa, sb = operands(batch, m, n, k, 0, 1, True, seed=31)
+    b8 = b.view(torch.uint8).clone()
+    b8[1, :80, :] = 0x7C  # +inf in E5M2
+    b = b8.view(torch.float8_e5m2)
+    out = run(fp8g, a, b, sa, sb)
+    ref, _ = oracle_mod.bmm_fp8(a.view(torch.uint8)[:1], b8[:1], sa[:1].numpy(), sb[:1].numpy(),
+                                0, 1)
+    got = out[:1].float().cpu().double().numpy()
+    assert np.isfinite(got).all()
+    assert_close(got.reshape(-1), ref.reshape(-1), "bmm batch 0 beside infinities in batch 1")
+
+
 def test_argument_errors(fp8g):
     a, b, sa, sb = operands(1, 128, 256, 200, 0, 0, False, seed=7)
     with pytest.raises(fp8g.Fp8gError) as e:
         run(fp8g, a, b, sa, sb)
     assert e.value.status == fp8g.ERR_INVALID_ARGUMENT and "k = 200" in str(e.value)
+    a, b, sa, sb = operands(1, 128, 200, 256, 0, 0, False, seed=7)
+    with pytest.raises(fp8g.Fp8gError) as e:
+        run(fp8g, a, b, sa, sb)
+    assert e.value.status == fp8g.ERR_INVALID_ARGUMENT and "n = 200" in str(e.value)
