@@ -47,19 +47,22 @@ __host__ __device__ inline int64_t moe_rows(int64_t tokens, int64_t top_k, int64
     return (tokens * top_k + 127 * experts + 127) / 128 * 128;
 }
 
-// One CTA.  Shared memory: counts, offsets and cursors of the experts.
+// One CTA.  Shared memory: counts, offsets and cursors of the experts.  The
+// slots are read twice (to count, then to place); m_indices is written from
+// the segments' offsets and counts in coalesced runs, not slot by slot.
 __global__ void __launch_bounds__(MOE_ROUTE_THREADS)
     moe_route_kernel(const int32_t* __restrict__ token_selected, int pairs, int experts,
                      int m_rows, int32_t* __restrict__ m_indices, int32_t* __restrict__ row_of,
                      unsigned int* status) {
     extern __shared__ int route_smem[];
+    __shared__ int warp_total[MOE_ROUTE_THREADS / 32];
     int* count = route_smem;
     int* offset = route_smem + experts;
     int* cursor = route_smem + 2 * experts;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     grid_dependency_wait();
     grid_launch_dependents();
     for (int e = threadIdx.x; e < experts; e += blockDim.x) count[e] = cursor[e] = 0;
-    for (int r = threadIdx.x; r < m_rows; r += blockDim.x) m_indices[r] = -1;
     __syncthreads();
     for (int p0 = threadIdx.x; p0 < pairs; p0 += blockDim.x * MOE_ROUTE_BATCH) {
         int e[MOE_ROUTE_BATCH];
@@ -77,12 +80,36 @@ __global__ void __launch_bounds__(MOE_ROUTE_THREADS)
         }
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int acc = 0;
-        for (int e = 0; e < experts; ++e) {
-            offset[e] = acc;
-            acc += (count[e] + 127) / 128 * 128;
+    // offsets: exclusive scan of the counts rounded up to 128, the experts split
+    // evenly over the threads (every thread runs the shuffles)
+    const int per = (experts + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(experts, static_cast<int>(threadIdx.x) * per);
+    const int e1 = min(experts, e0 + per);
+    int mine = 0;
+    for (int e = e0; e < e1; ++e) mine += (count[e] + 127) / 128 * 128;
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_total[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = static_cast<int>(blockDim.x) / 32;
+        int t = lane < nw ? warp_total[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += v;
         }
+        if (lane < nw) warp_total[lane] = t;  // inclusive over the warps
+    }
+    __syncthreads();
+    int acc = incl - mine + (warp > 0 ? warp_total[warp - 1] : 0);
+    for (int e = e0; e < e1; ++e) {
+        offset[e] = acc;
+        acc += (count[e] + 127) / 128 * 128;
     }
     __syncthreads();
     for (int p0 = threadIdx.x; p0 < pairs; p0 += blockDim.x * MOE_ROUTE_BATCH) {
@@ -97,13 +124,20 @@ __global__ void __launch_bounds__(MOE_ROUTE_THREADS)
             const int p = p0 + u * blockDim.x;
             if (p >= pairs) break;
             int row = -1;
-            if (e[u] >= 0 && e[u] < experts) {
-                row = offset[e[u]] + atomicAdd(&cursor[e[u]], 1);
-                m_indices[row] = e[u];
-            }
+            if (e[u] >= 0 && e[u] < experts) row = offset[e[u]] + atomicAdd(&cursor[e[u]], 1);
             row_of[p] = row;
         }
     }
+    // m_indices segment by segment, one warp per expert: its rows, then -1 up to
+    // the next multiple of 128; then -1 past the last segment
+    const int nwarps = static_cast<int>(blockDim.x) / 32;
+    for (int e = warp; e < experts; e += nwarps) {
+        const int start = offset[e], n = count[e], len = (n + 127) / 128 * 128;
+        for (int i = lane; i < len; i += 32) m_indices[start + i] = i < n ? e : -1;
+    }
+    const int total = offset[experts - 1] + (count[experts - 1] + 127) / 128 * 128;
+    for (int r = total + static_cast<int>(threadIdx.x); r < m_rows; r += blockDim.x)
+        m_indices[r] = -1;
 }
 
 // 1 x 128 quantisation of 8 FP32 values held by each of the 16 lanes of a
