@@ -151,9 +151,10 @@ __device__ __forceinline__ uint2 quantise_block_8(const float (&v)[8], unsigned 
     for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o));
     const bool zero = amax == 0.0f;
     scale = zero ? 0.0f : __fdiv_rn(amax, 448.0f);
+    const BlockDivisor div(scale);
     uint2 codes;
-    codes.x = e4m3_pair(v[0], v[1], scale, zero) | (e4m3_pair(v[2], v[3], scale, zero) << 16);
-    codes.y = e4m3_pair(v[4], v[5], scale, zero) | (e4m3_pair(v[6], v[7], scale, zero) << 16);
+    codes.x = e4m3_pair(v[0], v[1], div, zero) | (e4m3_pair(v[2], v[3], div, zero) << 16);
+    codes.y = e4m3_pair(v[4], v[5], div, zero) | (e4m3_pair(v[6], v[7], div, zero) << 16);
     return codes;
 }
 

@@ -61,11 +61,38 @@ __device__ __forceinline__ uint4 ld_once_v4(const uint4* p) {
     return v;
 }
 
+// Correctly rounded y / scale for the elements of one 1 x 128 block, by
+// Markstein's scheme (P. Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with r
+// the correctly rounded reciprocal of scale (once per block), q = y * r is
+// within two ulps of y / scale; a correction q += (y - scale q) r, whose
+// residual the FMA forms exactly, brings it within one ulp, and by
+// Markstein's theorem a second such correction rounds it correctly.  Where a
+// step could overflow or underflow (scale outside [2^-100, 2^100]) it falls
+// back to the IEEE division.  Quotients too small for the residual to be
+// exact lie far below the smallest E4M3 subnormal, where every candidate
+// gives the same code.
+struct BlockDivisor {
+    float b, r;
+    bool fast;
+    __device__ __forceinline__ explicit BlockDivisor(float scale) : b(scale) {
+        fast = scale >= 0x1p-100f && scale <= 0x1p+100f;
+        r = fast ? __frcp_rn(scale) : 0.0f;
+    }
+    __device__ __forceinline__ float operator()(float y) const {
+        if (!fast) return __fdiv_rn(y, b);
+        float q = y * r;
+        q = fmaf(fmaf(-b, q, y), r, q);
+        return fmaf(fmaf(-b, q, y), r, q);
+    }
+};
+
 // Two E4M3 codes of y0 / scale and y1 / scale (low byte first).
-__device__ __forceinline__ uint32_t e4m3_pair(float y0, float y1, float scale, bool zero) {
+__device__ __forceinline__ uint32_t e4m3_pair(float y0, float y1, const BlockDivisor& div,
+                                              bool zero) {
     float2 q;
-    q.x = zero ? 0.0f : __fdiv_rn(y0, scale);
-    q.y = zero ? 0.0f : __fdiv_rn(y1, scale);
+    q.x = zero ? 0.0f : div(y0);
+    q.y = zero ? 0.0f : div(y1);
     return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, __NV_E4M3));
 }
 
@@ -145,11 +172,12 @@ __global__ void __launch_bounds__(NQ_THREADS)
                 amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o));
             const bool zero = amax == 0.0f;
             const float scale = zero ? 0.0f : __fdiv_rn(amax, 448.0f);
+            const BlockDivisor div(scale);
             uint2 codes;
-            codes.x = e4m3_pair(bf16_lo(yw[0]), bf16_hi(yw[0]), scale, zero) |
-                      (e4m3_pair(bf16_lo(yw[1]), bf16_hi(yw[1]), scale, zero) << 16);
-            codes.y = e4m3_pair(bf16_lo(yw[2]), bf16_hi(yw[2]), scale, zero) |
-                      (e4m3_pair(bf16_lo(yw[3]), bf16_hi(yw[3]), scale, zero) << 16);
+            codes.x = e4m3_pair(bf16_lo(yw[0]), bf16_hi(yw[0]), div, zero) |
+                      (e4m3_pair(bf16_lo(yw[1]), bf16_hi(yw[1]), div, zero) << 16);
+            codes.y = e4m3_pair(bf16_lo(yw[2]), bf16_hi(yw[2]), div, zero) |
+                      (e4m3_pair(bf16_lo(yw[3]), bf16_hi(yw[3]), div, zero) << 16);
             o2[v] = codes;
             if (hl == 0) block_scale[static_cast<int64_t>(row) * nblk + blk] = scale;
         }
@@ -283,11 +311,12 @@ __global__ void __launch_bounds__(NQ_THREADS)
                 amax = fmaxf(amax, __shfl_xor_sync(half_mask, amax, o));
             const bool zero = amax == 0.0f;
             const float scale = zero ? 0.0f : __fdiv_rn(amax, 448.0f);
+            const BlockDivisor div(scale);
             uint2 codes;
-            codes.x = e4m3_pair(bf16_lo(yw[0]), bf16_hi(yw[0]), scale, zero) |
-                      (e4m3_pair(bf16_lo(yw[1]), bf16_hi(yw[1]), scale, zero) << 16);
-            codes.y = e4m3_pair(bf16_lo(yw[2]), bf16_hi(yw[2]), scale, zero) |
-                      (e4m3_pair(bf16_lo(yw[3]), bf16_hi(yw[3]), scale, zero) << 16);
+            codes.x = e4m3_pair(bf16_lo(yw[0]), bf16_hi(yw[0]), div, zero) |
+                      (e4m3_pair(bf16_lo(yw[1]), bf16_hi(yw[1]), div, zero) << 16);
+            codes.y = e4m3_pair(bf16_lo(yw[2]), bf16_hi(yw[2]), div, zero) |
+                      (e4m3_pair(bf16_lo(yw[3]), bf16_hi(yw[3]), div, zero) << 16);
             o2[v] = codes;
             if (hl == 0) block_scale[static_cast<int64_t>(row) * nblk + blk] = scale;
         }
