@@ -263,6 +263,30 @@ def test_stagewise_parity_small_layers(fp8g, oracle_mod, tokens, top_k, experts,
     _check_combine(oracle_mod, st, out)
 
 
+def test_quantise_gather_at_extreme_magnitudes(fp8g, oracle_mod):
+    # The 1 x 128 quantisation divides by the block scale with one reciprocal and
+    # two FMA corrections where the scale lies in [2^-100, 2^100], and by the IEEE
+    # division outside it.  Blocks of every token are scaled to both sides of
+    # both limits (and far past them); the codes and scales stay bit-exact.
+    tokens, top_k, experts, hidden, inter = 24, 2, 4, 768, 128
+    w = workloads.moe(tokens, top_k, experts, hidden, inter, seed=77)
+    x = w["input"].float()
+    exps = [-120.0, -95.0, -85.0, 0.0, 100.0, 110.0]  # per 128-column block
+    for b, e in enumerate(exps):
+        x[:, b * 128:(b + 1) * 128] *= 2.0 ** e
+    x[::5, 256:384] *= 2.0 ** 9   # straddle the lower limit from the other side
+    w["input"] = x.bfloat16()
+    assert torch.isfinite(w["input"].float()).all()
+    out, ws = _run_with_workspace(fp8g, w)
+    st = _stages(fp8g, w, ws)
+    ts = w["token_selected"].numpy()
+    _check_route(st, ts, experts)
+    _check_quant_gather(oracle_mod, st, w, ts)
+    s = st["a1_scale"][st["row_of"][ts >= 0]]
+    assert (s < 2.0 ** -100).any() and (s > 2.0 ** 100).any() and \
+        ((s > 2.0 ** -100) & (s < 2.0 ** 100)).any()
+
+
 def test_stagewise_parity_4096_tokens(fp8g, oracle_mod):
     w = workloads.make("moe_4096tok_top8_e64_h7168_i2048", device="cuda")
     out, ws = _run_with_workspace(fp8g, w)
