@@ -38,15 +38,28 @@ constexpr int BMM_STAGES = 4;
 constexpr int BMM_A_BYTES = BLOCK_M * BLOCK_K;         // 16 KB
 constexpr int BMM_B_HALF_BYTES = BLOCK_K * 128;        // 128 k-rows x 128 columns: 16 KB
 constexpr int BMM_B_BYTES = 2 * BMM_B_HALF_BYTES;      // the tile's 256 columns
-constexpr size_t BMM_SMEM_BYTES = 1024 + size_t(BMM_STAGES) * (BMM_A_BYTES + BMM_B_BYTES) +
-                                  2 * OUT_STAGE_BYTES + BAR_BYTES;
-static_assert(BMM_SMEM_BYTES <= 232448, "shared memory of the bmm kernel");
+
+// One CTA per 128 x 256 tile, or a CTA pair per 256 x 256 tile (cta_group::2:
+// each CTA loads its own 128 rows of A and one 128-column half of B, so each
+// SM moves a third fewer operand bytes per MMA).
+template <bool PAIR>
+struct BmmCfg {
+    static constexpr int TILE_M = PAIR ? 2 * BLOCK_M : BLOCK_M;
+    static constexpr int B_BYTES = PAIR ? BMM_B_HALF_BYTES : BMM_B_BYTES;  // per CTA
+    static constexpr int STAGE_BYTES = BMM_A_BYTES + B_BYTES;
+    static constexpr size_t SMEM_BYTES =
+        1024 + size_t(BMM_STAGES) * STAGE_BYTES + 2 * OUT_STAGE_BYTES + BAR_BYTES;
+    static_assert(SMEM_BYTES <= 232448, "shared memory of the bmm kernel");
+};
+constexpr size_t BMM_SMEM_BYTES = BmmCfg<false>::SMEM_BYTES;
 
 // Instruction descriptor of kind::f8f6f4: FP32 D; A (format a_fmt, K-major);
-// B (format b_fmt, MN-major); M = 128, N = 256.  Formats: 0 = E4M3, 1 = E5M2.
-__host__ __device__ constexpr uint32_t idesc_bmm(uint32_t a_fmt, uint32_t b_fmt) {
+// B (format b_fmt, MN-major); M = m (128, or 256 on a pair), N = 256.
+// Formats: 0 = E4M3, 1 = E5M2.
+__host__ __device__ constexpr uint32_t idesc_bmm(uint32_t a_fmt, uint32_t b_fmt,
+                                                 uint32_t m = 128) {
     return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | (0u << 15) | (1u << 16) |
-           ((256u >> 3) << 17) | ((128u >> 4) << 24);
+           ((256u >> 3) << 17) | ((m >> 4) << 24);
 }
 
 // Shared-memory descriptor of an MN-major operand with 128-byte swizzle: atoms
@@ -61,13 +74,15 @@ __device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t 
 
 struct BmmTile {
     int bb;     // batch
-    int rin0;   // first row of the tile within the batch
-    int row0;   // first row in the (batch * m) x k view of A (and of out)
+    int rin0;   // first row of this CTA's 128 within the batch
+    int row0;   // the same row in the (batch * m) x k view of A (and of out)
     int n0;     // first column
 };
 
-// Tile t: batch-major, then bands of band_m m-blocks with the m-block fastest.
-__device__ __forceinline__ bool bmm_tile(const Params& p, int t, BmmTile& tile) {
+// Tile t: batch-major, then bands of band_m m-blocks (of TILE_M rows) with the
+// m-block fastest.  `rank`: this CTA's half of a pair's 256 rows.
+template <bool PAIR>
+__device__ __forceinline__ bool bmm_tile(const Params& p, int t, int rank, BmmTile& tile) {
     if (t >= p.num_tiles) return false;
     const int per_batch = p.m_blocks * p.n_tiles;
     const int bb = t / per_batch;
@@ -79,35 +94,43 @@ __device__ __forceinline__ bool bmm_tile(const Params& p, int t, BmmTile& tile) 
     const int nb = rem / in_band;
     const int mb = band * p.band_m + rem % in_band;
     tile.bb = bb;
-    tile.rin0 = mb * BLOCK_M;
-    tile.row0 = bb * p.rows + mb * BLOCK_M;
+    tile.rin0 = mb * BmmCfg<PAIR>::TILE_M + rank * BLOCK_M;
+    tile.row0 = bb * p.rows + tile.rin0;
     tile.n0 = nb * BLOCK_N;
     return true;
 }
 
+template <bool PAIR>
 __device__ __forceinline__ void bmm_producer(const CUtensorMap* map_a, const CUtensorMap* map_b,
-                                             const Params& p, uint8_t* sA, uint8_t* sB,
+                                             const Params& p, int rank, uint8_t* sA, uint8_t* sB,
                                              uint64_t* full, uint64_t* empty, const Ctl& ctl) {
+    using C = BmmCfg<PAIR>;
     const int lane = threadIdx.x & 31;
     int stage = 0;
     uint32_t phase = 0, armed = 0, armed_parity = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok; t += gridDim.x) {
+    for (int t = tile_first<PAIR>(); ok; t += tile_stride<PAIR>()) {
         BmmTile tile;
-        if (!bmm_tile(p, t, tile)) break;
+        if (!bmm_tile<PAIR>(p, t, rank, tile)) break;
         if (lane == 0) {
             for (int kb = 0; kb < p.kblocks; ++kb) {
                 if (!wait_phase(empty + stage, phase ^ 1u, ctl)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(full + stage, BMM_A_BYTES + BMM_B_BYTES);
+                mbar_arrive_expect_tx(full + stage, C::STAGE_BYTES);
                 tma_load_2d(sA + stage * BMM_A_BYTES, map_a, full + stage, kb * BLOCK_K,
                             tile.row0);
-                uint8_t* b = sB + stage * BMM_B_BYTES;
-                tma_load_3d(b, map_b, full + stage, tile.n0, kb * BLOCK_K, tile.bb);
-                tma_load_3d(b + BMM_B_HALF_BYTES, map_b, full + stage, tile.n0 + 128,
-                            kb * BLOCK_K, tile.bb);
+                uint8_t* b = sB + stage * C::B_BYTES;
+                if constexpr (PAIR) {
+                    // this CTA's 128-column half of the pair's 256 columns
+                    tma_load_3d(b, map_b, full + stage, tile.n0 + rank * 128, kb * BLOCK_K,
+                                tile.bb);
+                } else {
+                    tma_load_3d(b, map_b, full + stage, tile.n0, kb * BLOCK_K, tile.bb);
+                    tma_load_3d(b + BMM_B_HALF_BYTES, map_b, full + stage, tile.n0 + 128,
+                                kb * BLOCK_K, tile.bb);
+                }
                 armed |= 1u << stage;
                 armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == BMM_STAGES) {
@@ -124,8 +147,37 @@ __device__ __forceinline__ void bmm_producer(const CUtensorMap* map_a, const CUt
     __syncwarp();
 }
 
-// Tile tl of this CTA goes to TMEM buffer tl mod 2, accumulating over the
-// whole of K; slots are taken in order j = 0, 1, 2, ...
+// Odd CTA of a pair: each time one of its slots has landed, arrive on the even
+// CTA's barrier of that slot, whose MMA warp then sees both halves land.
+__device__ __forceinline__ void bmm_relay(const Params& p, uint64_t* full, const Ctl& ctl) {
+    const int lane = threadIdx.x & 31;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = tile_first<true>(); ok; t += tile_stride<true>()) {
+        BmmTile tile;
+        if (!bmm_tile<true>(p, t, 1, tile)) break;
+        if (lane == 0) {
+            for (int kb = 0; kb < p.kblocks; ++kb) {
+                if (!wait_phase(full + stage, phase, ctl)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_remote(mapa_shared(full + stage, 0));
+                if (++stage == BMM_STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+}
+
+// Tile tl of this CTA (or pair: issued by the even CTA) goes to TMEM buffer
+// tl mod 2, accumulating over the whole of K; slots are taken in order
+// j = 0, 1, 2, ...
+template <bool PAIR>
 __device__ __forceinline__ void bmm_mma(const Params& p, uint8_t* sA, uint8_t* sB, uint64_t* full,
                                         uint64_t* empty, uint64_t* acc_full, uint64_t* acc_empty,
                                         uint64_t* drain, uint32_t tmem_base, const Ctl& ctl) {
@@ -135,9 +187,9 @@ __device__ __forceinline__ void bmm_mma(const Params& p, uint8_t* sA, uint8_t* s
     const int KB = p.kblocks;
     uint32_t j = 0, tl = 0;  // K blocks and tiles of this CTA so far
     bool ok = true;
-    for (int t = blockIdx.x; ok; t += gridDim.x, ++tl, j += KB) {
+    for (int t = tile_first<PAIR>(); ok; t += tile_stride<PAIR>(), ++tl, j += KB) {
         BmmTile tile;
-        if (!bmm_tile(p, t, tile)) break;
+        if (!bmm_tile<PAIR>(p, t, 0, tile)) break;
         if (lane == 0) {
             const int buf = static_cast<int>(tl & 1u);
             const uint32_t bphase = (tl >> 1) & 1u;
@@ -152,23 +204,39 @@ __device__ __forceinline__ void bmm_mma(const Params& p, uint8_t* sA, uint8_t* s
                 }
                 tc_fence_after_sync();
                 const uint64_t ad = a_desc0 + static_cast<uint64_t>((stage * BMM_A_BYTES) >> 4);
-                const uint32_t bs = b_base + stage * BMM_B_BYTES;
+                const uint32_t bs = b_base + stage * BmmCfg<PAIR>::B_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BLOCK_K / UMMA_K; ++kk) {
-                    // A: +32 bytes inside its swizzled rows; B: +32 k-rows (4 atoms)
+                    // A: +32 bytes inside its swizzled rows; B: +32 k-rows (4 atoms).
+                    // On a pair each CTA's B is one 128-column half (one atom wide).
                     const uint64_t bd = smem_desc_mn_sw128(bs + kk * UMMA_K * 128,
                                                            BMM_B_HALF_BYTES, 1024);
-                    umma_f8f6f4(d, ad + static_cast<uint64_t>((kk * UMMA_K) >> 4), bd, p.idesc,
-                                (kb > 0 || kk > 0) ? 1u : 0u);
+                    const uint64_t adk = ad + static_cast<uint64_t>((kk * UMMA_K) >> 4);
+                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                    if constexpr (PAIR)
+                        umma_f8f6f4_pair(d, adk, bd, p.idesc, acc);
+                    else
+                        umma_f8f6f4(d, adk, bd, p.idesc, acc);
                 }
-                umma_commit(empty + stage);
+                if constexpr (PAIR)
+                    umma_commit_pair_multicast(empty + stage, 0x3);  // both CTAs' slots
+                else
+                    umma_commit(empty + stage);
             }
-            if (ok) umma_commit(acc_full + buf);
+            if (ok) {
+                if constexpr (PAIR)
+                    umma_commit_pair_multicast(acc_full + buf, 0x3);  // both CTAs' rows
+                else
+                    umma_commit(acc_full + buf);
+            }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
     }
     if (lane == 0) {
-        umma_commit(drain);
+        if constexpr (PAIR)
+            umma_commit_pair(drain);
+        else
+            umma_commit(drain);
         drain_wait(drain, 0);
     }
     __syncwarp();
@@ -179,8 +247,8 @@ __device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
            (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
 }
 
-template <typename OutT>
-__device__ __forceinline__ void bmm_epilogue(const Params& p, uint64_t* acc_full,
+template <typename OutT, bool PAIR>
+__device__ __forceinline__ void bmm_epilogue(const Params& p, int rank, uint64_t* acc_full,
                                              uint64_t* acc_empty, uint32_t tmem_base,
                                              uint8_t* sOut, const Ctl& ctl) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -189,9 +257,9 @@ __device__ __forceinline__ void bmm_epilogue(const Params& p, uint64_t* acc_full
     const int r = quarter * 32 + lane;
     OutT* out = static_cast<OutT*>(p.out);
     uint32_t tl = 0;
-    for (int t = blockIdx.x;; t += gridDim.x, ++tl) {
+    for (int t = tile_first<PAIR>();; t += tile_stride<PAIR>(), ++tl) {
         BmmTile tile;
-        if (!bmm_tile(p, t, tile)) break;
+        if (!bmm_tile<PAIR>(p, t, rank, tile)) break;
         const int buf = static_cast<int>(tl & 1u);
         const uint32_t bphase = (tl >> 1) & 1u;
         const int rin = tile.rin0 + r;
@@ -237,7 +305,13 @@ __device__ __forceinline__ void bmm_epilogue(const Params& p, uint64_t* acc_full
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty + buf);
+            if (lane == 0) {
+                // a pair's buffers are reused by the even CTA's MMA warp
+                if constexpr (PAIR)
+                    mbar_arrive_remote(mapa_shared(acc_empty + buf, 0));
+                else
+                    mbar_arrive(acc_empty + buf);
+            }
         }
         if (col_ok)
             store_tile_rows<OutT>(out, p.n, out_row - r, col0, ok && row_ok, acc,
@@ -246,16 +320,17 @@ __device__ __forceinline__ void bmm_epilogue(const Params& p, uint64_t* acc_full
     }
 }
 
-template <typename OutT>
+template <typename OutT, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bmm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                const Params p) {
+    using C = BmmCfg<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = sA + BMM_STAGES * BMM_A_BYTES;
-    uint8_t* sOut = sB + BMM_STAGES * BMM_B_BYTES;
+    uint8_t* sOut = sB + BMM_STAGES * C::B_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 2 * OUT_STAGE_BYTES);
     uint64_t* empty = full + BMM_STAGES;
     uint64_t* acc_full = empty + BMM_STAGES;
@@ -265,14 +340,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
+    const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < BMM_STAGES; ++s) {
-            mbar_init(full + s, 1);
+            // the even CTA of a pair also counts the odd CTA's relay
+            mbar_init(full + s, (PAIR && rank == 0) ? 2 : 1);
             mbar_init(empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full + b, 1);
-            mbar_init(acc_empty + b, NUM_PROMO_WARPS);
+            mbar_init(acc_empty + b, PAIR ? 2 * NUM_PROMO_WARPS : NUM_PROMO_WARPS);
         }
         mbar_init(drain, 1);  // the MMA issuer's final commit
         *abort_flag = 0;
@@ -283,37 +360,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_map(&map_b);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(tmem_slot, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync();  // both CTAs' barriers exist before any cross-CTA signal
+    else
+        __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-    const Ctl ctl{abort_flag, 0u, p.status, p.wait_limit_ns};
+    const Ctl ctl{abort_flag, PAIR ? mapa_shared(abort_flag, rank ^ 1) : 0u, p.status,
+                  p.wait_limit_ns};
     grid_dependency_wait();
     grid_launch_dependents();
 
     if (warp < FIRST_PROMO_WARP) {
         regs_dec<CONTROL_REGS>();
-        if (warp == 0)
-            bmm_producer(&map_a, &map_b, p, sA, sB, full, empty, ctl);
-        else if (warp == 1)
-            bmm_mma(p, sA, sB, full, empty, acc_full, acc_empty, drain, tmem_base, ctl);
+        if (warp == 0) {
+            bmm_producer<PAIR>(&map_a, &map_b, p, rank, sA, sB, full, empty, ctl);
+        } else if (warp == 1) {
+            if (PAIR && rank == 1)
+                bmm_relay(p, full, ctl);
+            else
+                bmm_mma<PAIR>(p, sA, sB, full, empty, acc_full, acc_empty, drain, tmem_base, ctl);
+        }
     } else {
         regs_inc<PROMO_REGS>();
-        bmm_epilogue<OutT>(p, acc_full, acc_empty, tmem_base, sOut, ctl);
+        bmm_epilogue<OutT, PAIR>(p, rank, acc_full, acc_empty, tmem_base, sOut, ctl);
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync();  // no CTA leaves while the other may still signal it
+    else
+        __syncthreads();
     if (*reinterpret_cast<volatile int*>(abort_flag)) {
         abort_grace();
-        __syncthreads();
+        if constexpr (PAIR)
+            cluster_sync();
+        else
+            __syncthreads();
     }
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 

@@ -60,8 +60,9 @@ fp8g_status_t cuda_fail(cudaError_t e, const char* what) {
 
 constexpr int kMaxDevices = 64;
 // dense bf16, dense f16 (single CTA), grouped, masked, dense bf16, dense f16 (CTA pair),
-// dense E4M3 (single CTA), dense E4M3 (CTA pair), bmm bf16, bmm f16, masked (CTA pair)
-constexpr int kNumKernels = 11;
+// dense E4M3 (single CTA), dense E4M3 (CTA pair), bmm bf16, bmm f16, masked (CTA pair),
+// bmm bf16 (CTA pair), bmm f16 (CTA pair)
+constexpr int kNumKernels = 13;
 
 struct DeviceState {
     bool probed = false;
@@ -360,12 +361,27 @@ Params base_params(const float* a_scale, const float* b_scale, void* out, int64_
     return p;
 }
 
-// bmm_fp8 kernel launch (persistent, one CTA per SM) on validated arguments.
-template <typename OutT>
+// bmm_fp8 kernel launch (persistent, one CTA or CTA pair per SM or SM pair) on
+// validated arguments.
+template <typename OutT, bool PAIR>
 fp8g_status_t launch_bmm(DeviceState& ds, int slot, const CUtensorMap& map_a,
                          const CUtensorMap& map_b, const Params& p, int64_t tiles,
                          cudaStream_t stream) {
-    auto kernel = fp8g::bmm_kernel<OutT>;
+    using C = fp8g::BmmCfg<PAIR>;
+    auto kernel = fp8g::bmm_kernel<OutT, PAIR>;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = 2;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(fp8g::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attrs;
+    cfg.numAttrs = PAIR ? 2 : 1;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!ds.kernel_ready[slot]) {
@@ -377,23 +393,27 @@ fp8g_status_t launch_bmm(DeviceState& ds, int slot, const CUtensorMap& map_a,
                             "kernel built with %d registers per thread, expected %u", attr.numRegs,
                             fp8g::LAUNCH_REGS);
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(fp8g::BMM_SMEM_BYTES));
+                                     static_cast<int>(C::SMEM_BYTES));
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-            ds.resident[slot] = ds.sm_count;
+            int resident = ds.sm_count;
+            if (PAIR) {
+                cudaLaunchConfig_t occ = cfg;
+                occ.gridDim = dim3(2, 1, 1);
+                occ.attrs = &attrs[1];  // the cluster shape alone
+                occ.numAttrs = 1;
+                int clusters = 0;
+                e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &occ);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+                if (clusters < 1)
+                    return fail(FP8G_ERR_UNSUPPORTED, "no CTA pair of this kernel fits an SM pair");
+                resident = clusters;
+            }
+            ds.resident[slot] = resident;
             ds.kernel_ready[slot] = true;
         }
     }
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
     const int64_t units = tiles < ds.resident[slot] ? tiles : ds.resident[slot];
-    cfg.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
-    cfg.blockDim = dim3(fp8g::NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = fp8g::BMM_SMEM_BYTES;
-    cfg.stream = stream;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? 2 * units : units), 1, 1);
     (void)cudaGetLastError();
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, p);
     if (e == cudaSuccess) e = cudaGetLastError();
@@ -868,18 +888,30 @@ fp8g_status_t bmm_fp8(const void* a, const void* b, fp8g_fp8_format_t a_format,
                                   "b")) != FP8G_OK)
                 return s;
         }
-        Params p = base_params(a_scale, b_scale, out, m, n, k);
+        // CTA pairs on 256 x 256 tiles when there are enough of them to give every
+        // SM pair work (results are identical either way)
+        const int64_t pair_tiles = batch * ((m + 255) / 256) * n_tiles;
+        const bool pair = m > 128 && 2 * pair_tiles >= ds->sm_count;
+        const int tile_m = pair ? 2 * fp8g::BLOCK_M : fp8g::BLOCK_M;
+        const int64_t launch_tiles = pair ? pair_tiles : tiles;
+        Params p = base_params(a_scale, b_scale, out, m, n, k, tile_m);
         p.kblocks = static_cast<int>((k + fp8g::BLOCK_K - 1) / fp8g::BLOCK_K);
         p.band_m = 8;
-        p.num_tiles = static_cast<int>(tiles);
+        p.num_tiles = static_cast<int>(launch_tiles);
         p.batch = static_cast<int>(batch);
         p.a_channelwise = a_channelwise != 0;
         p.b_channelwise = b_channelwise != 0;
-        p.idesc = fp8g::idesc_bmm(static_cast<uint32_t>(a_format), static_cast<uint32_t>(b_format));
+        p.idesc = fp8g::idesc_bmm(static_cast<uint32_t>(a_format), static_cast<uint32_t>(b_format),
+                                  static_cast<uint32_t>(tile_m));
         p.status = ds->status;
+        t_last_gemm_pair = pair ? 1 : 0;
         if (out_dtype == FP8G_OUT_BF16)
-            return launch_bmm<__nv_bfloat16>(*ds, 8, map_a, map_b, p, tiles, stream);
-        return launch_bmm<__half>(*ds, 9, map_a, map_b, p, tiles, stream);
+            return pair ? launch_bmm<__nv_bfloat16, true>(*ds, 11, map_a, map_b, p, launch_tiles,
+                                                           stream)
+                        : launch_bmm<__nv_bfloat16, false>(*ds, 8, map_a, map_b, p, launch_tiles,
+                                                            stream);
+        return pair ? launch_bmm<__half, true>(*ds, 12, map_a, map_b, p, launch_tiles, stream)
+                    : launch_bmm<__half, false>(*ds, 9, map_a, map_b, p, launch_tiles, stream);
     } catch (...) {
         return fail(FP8G_ERR_CUDA, "unexpected exception");
     }

@@ -25,10 +25,10 @@ extern "C" {
 void fp8g_testing_set_wait_limit_ns(uint64_t ns);
 
 /*
- * Tile shape of the calling thread's last fp8_gemm_nt_groupwise launch: 1 if
- * it ran on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2), 0 if on one
- * CTA per 128 x 256 tile, -1 if the thread has launched none.  The shape never
- * changes results; this tells a test which one mma_sm chose.
+ * Tile shape of the calling thread's last fp8_gemm_nt_groupwise or bmm_fp8
+ * launch: 1 if it ran on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2), 0
+ * if on one CTA per 128 x 256 tile, -1 if the thread has launched none.  The
+ * shape never changes results; this tells a test which one was chosen.
  */
 int fp8g_testing_last_gemm_cta_pair(void);
 

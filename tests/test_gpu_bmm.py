@@ -132,6 +132,27 @@ def test_ragged_n_and_k_parity_and_no_write_past_the_output(fp8g, oracle_mod, a_
                  "bmm ragged %s %s %s" % (shape, a_fmt, b_fmt))
 
 
+@pytest.mark.parametrize("a_fmt,b_fmt", [(0, 0), (1, 0)])
+def test_cta_pairs_ragged_full_parity_and_same_bits_as_one_cta(fp8g, oracle_mod, a_fmt, b_fmt):
+    # enough 256 x 256 tiles for CTA pairs (each CTA 128 rows of A, one
+    # 128-column half of B); m, n and k ragged; full parity, and the same bits
+    # as the one-CTA kernel on the same batches (a problem too small for pairs,
+    # run batch by batch)
+    lib = fp8g.load()
+    batch, m, n, k = 3, 777, 2000, 1040
+    a, b, sa, sb = operands(batch, m, n, k, a_fmt, b_fmt, True, seed=61 + a_fmt)
+    out = run(fp8g, a, b, sa, sb)
+    assert lib.fp8g_testing_last_gemm_cta_pair() == 1
+    ref, _ = oracle_mod.bmm_fp8(a.view(torch.uint8), b.view(torch.uint8), sa.numpy(), sb.numpy(),
+                                a_fmt, b_fmt)
+    assert_close(out.float().cpu().double().numpy().reshape(-1), ref.reshape(-1),
+                 "bmm pairs %s %s" % (a_fmt, b_fmt))
+    for bb in range(batch):
+        one = run(fp8g, a[bb:bb + 1, :200], b[bb:bb + 1], sa[bb:bb + 1, :200], sb[bb:bb + 1])
+        assert lib.fp8g_testing_last_gemm_cta_pair() == 0
+        assert torch.equal(one.view(torch.int16)[0], out.view(torch.int16)[bb, :200])
+
+
 def test_k_tail_reads_no_row_of_the_next_batch(fp8g, oracle_mod):
     # k = 176: the last K block covers k-rows 128..255 of each batch.  The rows
     # past k must read as zero, not as the next batch's first rows: plant
