@@ -34,7 +34,6 @@
 
 namespace fp8g {
 
-constexpr int BMM_STAGES = 4;
 constexpr int BMM_A_BYTES = BLOCK_M * BLOCK_K;         // 16 KB
 constexpr int BMM_B_HALF_BYTES = BLOCK_K * 128;        // 128 k-rows x 128 columns: 16 KB
 constexpr int BMM_B_BYTES = 2 * BMM_B_HALF_BYTES;      // the tile's 256 columns
@@ -44,11 +43,13 @@ constexpr int BMM_B_BYTES = 2 * BMM_B_HALF_BYTES;      // the tile's 256 columns
 // SM moves a third fewer operand bytes per MMA).
 template <bool PAIR>
 struct BmmCfg {
+    // ring slots: a pair's slots are a third smaller; six measured 4% faster than four
+    static constexpr int STAGES = PAIR ? 6 : 4;
     static constexpr int TILE_M = PAIR ? 2 * BLOCK_M : BLOCK_M;
     static constexpr int B_BYTES = PAIR ? BMM_B_HALF_BYTES : BMM_B_BYTES;  // per CTA
     static constexpr int STAGE_BYTES = BMM_A_BYTES + B_BYTES;
     static constexpr size_t SMEM_BYTES =
-        1024 + size_t(BMM_STAGES) * STAGE_BYTES + 2 * OUT_STAGE_BYTES + BAR_BYTES;
+        1024 + size_t(STAGES) * STAGE_BYTES + 2 * OUT_STAGE_BYTES + BAR_BYTES;
     static_assert(SMEM_BYTES <= 232448, "shared memory of the bmm kernel");
 };
 constexpr size_t BMM_SMEM_BYTES = BmmCfg<false>::SMEM_BYTES;
@@ -133,7 +134,7 @@ __device__ __forceinline__ void bmm_producer(const CUtensorMap* map_a, const CUt
                 }
                 armed |= 1u << stage;
                 armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == BMM_STAGES) {
+                if (++stage == C::STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -142,7 +143,7 @@ __device__ __forceinline__ void bmm_producer(const CUtensorMap* map_a, const CUt
         ok = __shfl_sync(0xffffffffu, ok, 0);
     }
     if (lane == 0)
-        for (int s = 0; s < BMM_STAGES; ++s)
+        for (int s = 0; s < C::STAGES; ++s)
             if ((armed >> s) & 1u) drain_wait(full + s, (armed_parity >> s) & 1u);
     __syncwarp();
 }
@@ -164,7 +165,7 @@ __device__ __forceinline__ void bmm_relay(const Params& p, uint64_t* full, const
                     break;
                 }
                 mbar_arrive_remote(mapa_shared(full + stage, 0));
-                if (++stage == BMM_STAGES) {
+                if (++stage == BmmCfg<true>::STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -196,8 +197,8 @@ __device__ __forceinline__ void bmm_mma(const Params& p, uint8_t* sA, uint8_t* s
             const uint32_t d = tmem_base + static_cast<uint32_t>(buf * BLOCK_N);
             ok = wait_phase(acc_empty + buf, bphase ^ 1u, ctl);
             for (int kb = 0; ok && kb < KB; ++kb) {
-                const uint32_t stage = (j + kb) % BMM_STAGES;
-                const uint32_t phase = ((j + kb) / BMM_STAGES) & 1u;
+                const uint32_t stage = (j + kb) % BmmCfg<PAIR>::STAGES;
+                const uint32_t phase = ((j + kb) / BmmCfg<PAIR>::STAGES) & 1u;
                 if (!wait_phase(full + stage, phase, ctl)) {
                     ok = false;
                     break;
@@ -329,11 +330,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
-    uint8_t* sB = sA + BMM_STAGES * BMM_A_BYTES;
-    uint8_t* sOut = sB + BMM_STAGES * C::B_BYTES;
+    uint8_t* sB = sA + C::STAGES * BMM_A_BYTES;
+    uint8_t* sOut = sB + C::STAGES * C::B_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 2 * OUT_STAGE_BYTES);
-    uint64_t* empty = full + BMM_STAGES;
-    uint64_t* acc_full = empty + BMM_STAGES;
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* acc_full = empty + C::STAGES;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < BMM_STAGES; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
             // the even CTA of a pair also counts the odd CTA's relay
             mbar_init(full + s, (PAIR && rank == 0) ? 2 : 1);
             mbar_init(empty + s, 1);
